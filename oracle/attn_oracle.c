@@ -1,0 +1,225 @@
+/*
+ * CPU fp64 oracle for the fused attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header or constant with the CUDA path.
+ *
+ * What it computes is the plain definition of masked softmax attention, not
+ * the tiled algorithm that reaches it:
+ *
+ *   for every (b, h, i):
+ *     A(i)  = the attended key set of row i
+ *               dense           : all j in [0, L)
+ *               causal          : j <= i              ("Fused Attention" page,
+ *                                                      stage-2 mask offs_m >= offs_n)
+ *               block-diagonal  : floor(j/bs) == floor(i/bs)
+ *                                                     ("TLX Block Attention" page,
+ *                                                      definition of the diagonal
+ *                                                      blocks at its top)
+ *     s_j   = sm_scale * sum_d q[i,d] * k[j,d]     for j in A(i), ascending d
+ *     m     = max_{j in A(i)} s_j
+ *     l     = sum_{j in A(i)} exp(s_j - m)          (denominator starts at 0)
+ *     O[i,:]= sum_{j in A(i)} exp(s_j - m) * v[j,:] / l
+ *     lse_i = m + ln(l)                              ("Fused Attention" page,
+ *                                                      epilogue m_i += log(l_i))
+ *
+ * The scores of one row are all computed and held in an L-long buffer before
+ * the row is normalised (two passes over the row, no online update, no tiling
+ * over j).  Everything is fp64; the inputs are the fp16/bf16 values the GPU
+ * sees, widened exactly.  Rows are independent, so rows are spread over
+ * OpenMP threads; the arithmetic inside a row is strictly sequential.
+ *
+ * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake; the
+ * CPU tests build every mutant and check that the pins catch each of them.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+enum { OR_DENSE = 0, OR_CAUSAL = 1, OR_BLOCK_DIAG = 2 };
+enum { OR_F16 = 0, OR_BF16 = 1 };
+
+/* IEEE 754 binary16 -> double, from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double widen_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -24);               /* subnormal: f * 2^-14 * 2^-10 */
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + f), e - 25);   /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+/* bfloat16 -> double: bfloat16 is the upper half of an IEEE binary32. */
+static double widen_bf16(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+double attn_oracle_widen(uint16_t bits, int dtype)
+{
+    return dtype == OR_BF16 ? widen_bf16(bits) : widen_f16(bits);
+}
+
+/* 1 if key j is in the attended set of query row i. */
+static int attended(long i, long j, int mask_kind, long bs)
+{
+#if ORACLE_MUTANT == 1
+    if (mask_kind == OR_CAUSAL) return j < i;          /* planted: drops the diagonal */
+#endif
+#if ORACLE_MUTANT == 6
+    if (mask_kind == OR_BLOCK_DIAG) return (j % bs) == (i % bs);  /* planted: strided blocks */
+#endif
+    if (mask_kind == OR_CAUSAL) return j <= i;
+    if (mask_kind == OR_BLOCK_DIAG) return (j / bs) == (i / bs);
+    return 1;
+}
+
+/* One query row (b,h,i): fills o[0..D) and *lse.  q, k, v point at the
+ * (b,h) slice [L, D] already widened to fp64; s is scratch of length L. */
+static void one_row(const double *q, const double *k, const double *v,
+                    long L, long D, long i, int mask_kind, long bs,
+                    double sm_scale, double *s, double *o, double *lse)
+{
+    const double *qi = q + i * D;
+    double m = -INFINITY;
+    for (long j = 0; j < L; ++j) {
+        if (!attended(i, j, mask_kind, bs)) {
+            s[j] = -INFINITY;
+            continue;
+        }
+#if ORACLE_MUTANT == 7
+        const double *kj = v + j * D;                   /* planted: V in place of K */
+#else
+        const double *kj = k + j * D;
+#endif
+        double dot = 0.0;
+#if ORACLE_MUTANT == 10
+        for (long d = 0; d < D - 1; ++d)                /* planted: drops the last term */
+#else
+        for (long d = 0; d < D; ++d)
+#endif
+            dot += qi[d] * kj[d];
+#if ORACLE_MUTANT == 2
+        s[j] = dot;                                     /* planted: scale dropped */
+#else
+        s[j] = sm_scale * dot;
+#endif
+        if (s[j] > m) m = s[j];
+    }
+
+#if ORACLE_MUTANT == 3
+    double l = 1.0;                                     /* planted: denominator starts at 1 */
+#else
+    double l = 0.0;
+#endif
+    for (long d = 0; d < D; ++d) o[d] = 0.0;
+    for (long j = 0; j < L; ++j) {
+        if (s[j] == -INFINITY) continue;
+        double p = exp(s[j] - m);
+        l += p;
+#if ORACLE_MUTANT == 5
+        const double *vj = v + i * D;                   /* planted: wrong row of V */
+#elif ORACLE_MUTANT == 7
+        const double *vj = k + j * D;
+#else
+        const double *vj = v + j * D;
+#endif
+#if ORACLE_MUTANT == 9
+        p = exp(s[j]);                                  /* planted: max not removed in O only */
+#endif
+        for (long d = 0; d < D; ++d) o[d] += p * vj[d];
+    }
+    for (long d = 0; d < D; ++d) o[d] /= l;
+#if ORACLE_MUTANT == 4
+    *lse = log(l);                                      /* planted: max dropped from lse */
+#elif ORACLE_MUTANT == 8
+    *lse = m + log2(l);                                 /* planted: wrong log base */
+#else
+    *lse = m + log(l);
+#endif
+}
+
+/*
+ * Masked attention forward on [B,H,L,D] inputs given as raw fp16/bf16 bits.
+ *
+ *   rows == NULL : every row; O is [B,H,L,D] and lse is [B,H,L] (fp64).
+ *   rows != NULL : only the nrows flat row ids r = (b*H + h)*L + i; O is
+ *                  [nrows, D] and lse is [nrows], in the order given.
+ *
+ * Returns 0, or -1 on an argument error (nothing written).
+ */
+int attn_oracle(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                int dtype, long B, long H, long L, long D,
+                int mask_kind, long bs, double sm_scale,
+                const long *rows, long nrows,
+                double *O, double *lse, int nthreads)
+{
+    if (B < 0 || H < 0 || L < 0 || D <= 0) return -1;
+    if (mask_kind < OR_DENSE || mask_kind > OR_BLOCK_DIAG) return -1;
+    if (mask_kind == OR_BLOCK_DIAG && (bs <= 0 || (L > 0 && L % bs != 0))) return -1;
+    if (dtype != OR_F16 && dtype != OR_BF16) return -1;
+    const long BH = B * H;
+    const long total = rows ? nrows : BH * L;
+    if (total == 0) return 0;
+    if (rows)
+        for (long r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= BH * L) return -1;
+
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+    /* Rows are grouped by (b,h): each group widens its slice once. */
+#pragma omp parallel
+    {
+        double *qs = malloc(sizeof(double) * L * D);
+        double *ks = malloc(sizeof(double) * L * D);
+        double *vs = malloc(sizeof(double) * L * D);
+        double *s = malloc(sizeof(double) * (L > 0 ? L : 1));
+        long cur_bh = -1;
+        if (!qs || !ks || !vs || !s) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long t = 0; t < total; ++t) {
+            if (err) continue;
+            long r = rows ? rows[t] : t;
+            long bh = r / L, i = r % L;
+            if (bh != cur_bh) {
+                const size_t base = (size_t)bh * L * D;
+                for (long e = 0; e < L * D; ++e) {
+                    qs[e] = attn_oracle_widen(q[base + e], dtype);
+                    ks[e] = attn_oracle_widen(k[base + e], dtype);
+                    vs[e] = attn_oracle_widen(v[base + e], dtype);
+                }
+                cur_bh = bh;
+            }
+            one_row(qs, ks, vs, L, D, i, mask_kind, bs, sm_scale, s,
+                    O + (size_t)t * D, lse + t);
+        }
+        free(qs); free(ks); free(vs); free(s);
+    }
+    return err ? -1 : 0;
+}

@@ -1,0 +1,342 @@
+"""Pins for the CPU fp64 oracle: checks against facts that do not come from
+the oracle itself (closed forms, special cases that reduce to a textbook or
+library routine, brute force on tiny inputs, invariants of softmax attention).
+
+Every pin is a plain function taking an ``attn(q, k, v, mask, bs, scale,
+rows=None) -> (O, lse)`` callable.  ``test_pins`` runs them on the real
+oracle; ``test_planted_mistakes_are_caught`` builds each planted-mistake
+mutant of the oracle (a dropped term, a wrong index, a swapped operand, a wrong
+mask, ...) and checks that at least one pin fails for every one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_inputs import BLOCK_DIAG, CAUSAL, DENSE, make_qkv
+
+TOL = 1e-12
+
+
+def _attn_for(mutant=0):
+    def attn(q, k, v, mask, bs, scale, rows=None):
+        return oracle.attention(q, k, v, mask, bs, scale, rows=rows, nthreads=2, mutant=mutant)
+    return attn
+
+
+def _ints(shape, lo, hi, seed, dtype=torch.float16):
+    """Small integers (exact in fp16 and bf16) for pins that need exact sums."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, shape, generator=g).to(dtype)
+
+
+def _mask_matrix(L, mask, bs):
+    """The attended set written out directly from its definition."""
+    i = torch.arange(L)[:, None]
+    j = torch.arange(L)[None, :]
+    if mask == DENSE:
+        return torch.ones(L, L, dtype=torch.bool)
+    if mask == CAUSAL:
+        return j <= i
+    return (j // bs) == (i // bs)
+
+
+def _torch_ref(q, k, v, mask, bs, scale):
+    """Library special case: torch CPU fp64 softmax / logsumexp on the full matrix."""
+    qd, kd, vd = q.double(), k.double(), v.double()
+    s = torch.matmul(qd, kd.transpose(-1, -2)) * float(np.float32(scale))
+    s = s.masked_fill(~_mask_matrix(q.shape[2], mask, bs), float("-inf"))
+    return (torch.softmax(s, dim=-1) @ vd).numpy(), torch.logsumexp(s, dim=-1).numpy()
+
+
+# ----------------------------------------------------------------------------- pins
+
+def pin_torch_library(attn):
+    for mask, bs in [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 8), (BLOCK_DIAG, 5)]:
+        for dt in (torch.float16, torch.bfloat16):
+            L = 40
+            q, k, v = make_qkv(2, 2, L, 24, dt, seed=7 + mask)
+            O, lse = attn(q, k, v, mask, bs, 0.3)
+            Ot, lt = _torch_ref(q, k, v, mask, bs, 0.3)
+            assert np.abs(O - Ot).max() < TOL, (mask, bs, dt)
+            assert np.abs(lse - lt).max() < TOL, (mask, bs, dt)
+
+
+def _brute_row(qi, K, V, idx, scale):
+    """Pure-Python softmax attention of one row over the key indices idx."""
+    s = [scale * math.fsum(a * b for a, b in zip(qi, K[j])) for j in idx]
+    m = max(s)
+    w = [math.exp(x - m) for x in s]
+    l = math.fsum(w)
+    o = [math.fsum(w[t] * V[j][d] for t, j in enumerate(idx)) / l for d in range(len(V[0]))]
+    return o, m + math.log(l)
+
+
+def pin_brute_force(attn):
+    for mask, bs in [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 3), (BLOCK_DIAG, 1)]:
+        L, D = 12, 8
+        q, k, v = make_qkv(1, 2, L, D, torch.float16, seed=3)
+        scale = float(np.float32(0.41))
+        O, lse = attn(q, k, v, mask, bs, scale)
+        for h in range(2):
+            Q = q[0, h].double().tolist()
+            K = k[0, h].double().tolist()
+            V = v[0, h].double().tolist()
+            for i in range(L):
+                if mask == DENSE:
+                    idx = list(range(L))
+                elif mask == CAUSAL:
+                    idx = list(range(i + 1))
+                else:
+                    idx = list(range((i // bs) * bs, (i // bs + 1) * bs))
+                o, ls = _brute_row(Q[i], K, V, idx, scale)
+                assert np.abs(O[0, h, i] - np.array(o)).max() < TOL, (mask, h, i)
+                assert abs(lse[0, h, i] - ls) < TOL, (mask, h, i)
+
+
+def pin_brute_force_page_selfcheck(attn):
+    """Brute force on the full self-check shape of the TLX Block Attention page
+    (B=1, H=2, N=256, D=128, block 64, fp16, N(0,1), seed 42), sampled rows."""
+    q, k, v = make_qkv(1, 2, 256, 128, torch.float16, seed=42)
+    scale = float(np.float32(1.0 / math.sqrt(128)))
+    O, lse = attn(q, k, v, BLOCK_DIAG, 64, scale)
+    for h in range(2):
+        Q = q[0, h].double().tolist()
+        K = k[0, h].double().tolist()
+        V = v[0, h].double().tolist()
+        for i in (0, 1, 63, 64, 100, 191, 192, 255):
+            idx = list(range((i // 64) * 64, (i // 64 + 1) * 64))
+            o, ls = _brute_row(Q[i], K, V, idx, scale)
+            assert np.abs(O[0, h, i] - np.array(o)).max() < TOL
+            assert abs(lse[0, h, i] - ls) < TOL
+
+
+def pin_hand_example(attn):
+    """Closed form: q0=(1,0), keys k_j=(j,0), values v0=(1,0), v1=(0,1), v2=(0,0),
+    sm_scale=1.  Scores of row 0 are 0, 1, 2, so the weights are
+    1 : e : e^2 and lse = ln(1 + e + e^2).  Row 1 has q1=(0,1): every score is 0,
+    so the output is the plain mean of the attended values."""
+    q = torch.tensor([[1, 0], [0, 1], [1, 0]], dtype=torch.float16).view(1, 1, 3, 2)
+    k = torch.tensor([[0, 0], [1, 0], [2, 0]], dtype=torch.float16).view(1, 1, 3, 2)
+    v = torch.tensor([[1, 0], [0, 1], [0, 0]], dtype=torch.float16).view(1, 1, 3, 2)
+    e = math.e
+    z = 1 + e + e * e
+    O, lse = attn(q, k, v, DENSE, 0, 1.0)
+    assert abs(O[0, 0, 0, 0] - 1 / z) < TOL and abs(O[0, 0, 0, 1] - e / z) < TOL
+    assert abs(lse[0, 0, 0] - math.log(z)) < TOL
+    assert abs(O[0, 0, 1, 0] - 1 / 3) < TOL and abs(O[0, 0, 1, 1] - 1 / 3) < TOL
+    assert abs(lse[0, 0, 1] - math.log(3)) < TOL
+    O, lse = attn(q, k, v, CAUSAL, 0, 1.0)
+    assert O[0, 0, 0, 0] == 1 and O[0, 0, 0, 1] == 0 and lse[0, 0, 0] == 0
+    assert abs(O[0, 0, 1, 0] - 0.5) < TOL and abs(O[0, 0, 1, 1] - 0.5) < TOL
+    assert abs(lse[0, 0, 1] - math.log(2)) < TOL
+    # row 2 = row 0 under causal (it sees all three keys)
+    assert abs(O[0, 0, 2, 1] - e / z) < TOL and abs(lse[0, 0, 2] - math.log(z)) < TOL
+
+
+def pin_block_size_L_is_dense(attn):
+    q, k, v = make_qkv(1, 3, 48, 16, torch.bfloat16, seed=11)
+    O1, l1 = attn(q, k, v, BLOCK_DIAG, 48, 0.25)
+    O2, l2 = attn(q, k, v, DENSE, 0, 0.25)
+    assert np.array_equal(O1, O2) and np.array_equal(l1, l2)
+
+
+def pin_block_size_one_is_V(attn):
+    q, k, v = make_qkv(2, 1, 20, 8, torch.float16, seed=5)
+    scale = float(np.float32(0.7))
+    O, lse = attn(q, k, v, BLOCK_DIAG, 1, scale)
+    assert np.array_equal(O, v.double().numpy())
+    qk = (q.double() * k.double()).sum(-1).numpy()
+    assert np.abs(lse - scale * qk).max() < TOL
+
+
+def pin_block_decomposition(attn):
+    bs = 8
+    q, k, v = make_qkv(1, 2, 32, 16, torch.float16, seed=13)
+    O, lse = attn(q, k, v, BLOCK_DIAG, bs, 0.2)
+    for b0 in range(0, 32, bs):
+        sl = slice(b0, b0 + bs)
+        Os, ls = attn(q[:, :, sl].contiguous(), k[:, :, sl].contiguous(),
+                      v[:, :, sl].contiguous(), DENSE, 0, 0.2)
+        assert np.abs(O[:, :, sl] - Os).max() < TOL and np.abs(lse[:, :, sl] - ls).max() < TOL
+
+
+def pin_causal_rows(attn):
+    q, k, v = make_qkv(1, 2, 33, 16, torch.bfloat16, seed=17)
+    scale = float(np.float32(0.35))
+    O, lse = attn(q, k, v, CAUSAL, 0, scale)
+    Od, ld = attn(q, k, v, DENSE, 0, scale)
+    assert np.array_equal(O[:, :, 0], v[:, :, 0].double().numpy())
+    qk0 = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1).numpy()
+    assert np.abs(lse[:, :, 0] - scale * qk0).max() < TOL
+    assert np.abs(O[:, :, -1] - Od[:, :, -1]).max() < TOL
+    assert np.abs(lse[:, :, -1] - ld[:, :, -1]).max() < TOL
+    q1, k1, v1 = make_qkv(2, 2, 1, 8, torch.float16, seed=19)
+    for mask, bs in [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 1)]:
+        O1, _ = attn(q1, k1, v1, mask, bs, scale)
+        assert np.array_equal(O1, v1.double().numpy())
+
+
+def _attended_count(L, mask, bs):
+    return _mask_matrix(L, mask, bs).sum(-1).numpy()
+
+
+def pin_constant_keys(attn):
+    """All keys equal to kbar: every attended score of a row is the same, so
+    O_i is the plain mean of the attended V rows and lse_i = s q_i.kbar + ln|A(i)|."""
+    L, D = 24, 8
+    for mask, bs in [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 6)]:
+        q = _ints((1, 2, L, D), -3, 3, seed=23)
+        kbar = _ints((1, 2, 1, D), -2, 2, seed=29)
+        k = kbar.expand(1, 2, L, D).contiguous()
+        v = _ints((1, 2, L, D), -8, 8, seed=31)
+        O, lse = attn(q, k, v, mask, bs, 0.125)
+        M = _mask_matrix(L, mask, bs).double()
+        mean = (M @ v.double()) / M.sum(-1, keepdim=True)
+        assert np.abs(O - mean.numpy()).max() < TOL, mask
+        qk = (q.double() * kbar.double()).sum(-1).numpy()
+        expect = 0.125 * qk + np.log(_attended_count(L, mask, bs))
+        assert np.abs(lse - expect).max() < TOL, mask
+
+
+def pin_shift_and_affine(attn):
+    """K + 1 u^T leaves O unchanged and shifts lse_i by s q_i.u;
+    V -> a V + b maps O -> a O + b."""
+    L, D = 20, 8
+    for mask, bs in [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 4)]:
+        q = _ints((1, 1, L, D), -3, 3, seed=37)
+        k = _ints((1, 1, L, D), -3, 3, seed=41)
+        v = _ints((1, 1, L, D), -6, 6, seed=43)
+        u = _ints((1, 1, 1, D), -2, 2, seed=47)
+        O, lse = attn(q, k, v, mask, bs, 0.25)
+        O2, lse2 = attn(q, (k + u).contiguous(), v, mask, bs, 0.25)
+        shift = 0.25 * (q.double() * u.double()).sum(-1).numpy()
+        assert np.abs(O2 - O).max() < 1e-11, mask
+        assert np.abs(lse2 - (lse + shift)).max() < 1e-11, mask
+        O3, lse3 = attn(q, k, (2 * v + 0.5).contiguous(), mask, bs, 0.25)
+        assert np.abs(O3 - (2 * O + 0.5)).max() < 1e-11, mask
+        assert np.array_equal(lse3, lse)
+
+
+def pin_bounds(attn):
+    """O_i lies in the convex hull of the attended V rows; lse_i lies between
+    the row max m and m + ln|A(i)|."""
+    L = 30
+    for mask, bs in [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 10)]:
+        q, k, v = make_qkv(1, 2, L, 16, torch.float16, seed=53)
+        O, lse = attn(q, k, v, mask, bs, 0.5)
+        M = _mask_matrix(L, mask, bs)
+        vd = v.double()[0]
+        s = (q.double()[0] @ k.double()[0].transpose(-1, -2)) * 0.5
+        for h in range(2):
+            for i in range(L):
+                rows = vd[h][M[i]]
+                assert np.all(O[0, h, i] >= rows.min(0).values.numpy() - TOL)
+                assert np.all(O[0, h, i] <= rows.max(0).values.numpy() + TOL)
+                m = s[h, i][M[i]].max().item()
+                assert m - TOL <= lse[0, h, i] <= m + math.log(int(M[i].sum())) + TOL
+
+
+def pin_key_permutation(attn):
+    q, k, v = make_qkv(1, 2, 26, 16, torch.bfloat16, seed=59)
+    perm = torch.randperm(26, generator=torch.Generator().manual_seed(61))
+    O, lse = attn(q, k, v, DENSE, 0, 0.3)
+    O2, lse2 = attn(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), DENSE, 0, 0.3)
+    assert np.abs(O - O2).max() < TOL and np.abs(lse - lse2).max() < TOL
+
+
+PINS = [pin_torch_library, pin_brute_force, pin_brute_force_page_selfcheck, pin_hand_example,
+        pin_block_size_L_is_dense, pin_block_size_one_is_V, pin_block_decomposition,
+        pin_causal_rows, pin_constant_keys, pin_shift_and_affine, pin_bounds,
+        pin_key_permutation]
+
+
+# ----------------------------------------------------------------------------- tests
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pins(pin):
+    pin(_attn_for(0))
+
+
+def test_widen_all_fp16_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.widen(int(b), oracle.F16) for b in bits])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_widen_all_bf16_patterns():
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    want = bits.view(torch.bfloat16).double().numpy()
+    got = np.array([oracle.widen(int(b) & 0xFFFF, oracle.BF16) for b in bits.tolist()])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_row_subset_matches_full():
+    q, k, v = make_qkv(2, 3, 64, 32, torch.float16, seed=67)
+    O, lse = oracle.attention(q, k, v, CAUSAL, 0, 0.2)
+    rows = [5, 64 * 3 + 17, 64 * 6 - 1, 0, 64 * 4]
+    Or, lr = oracle.attention(q, k, v, CAUSAL, 0, 0.2, rows=rows)
+    Of, lf = O.reshape(-1, 32), lse.reshape(-1)
+    assert np.array_equal(Or, Of[rows]) and np.array_equal(lr, lf[rows])
+
+
+def test_rejects_bad_arguments():
+    q, k, v = make_qkv(1, 1, 12, 8, torch.float16)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, BLOCK_DIAG, 5, 0.1)       # 5 does not divide 12
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, BLOCK_DIAG, 0, 0.1)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, 3, 0, 0.1)
+
+
+def test_empty_inputs():
+    q, k, v = make_qkv(1, 2, 0, 8, torch.float16)
+    O, lse = oracle.attention(q, k, v, DENSE, 0, 0.1)
+    assert O.shape == (1, 2, 0, 8) and lse.shape == (1, 2, 0)
+
+
+MUTANTS = {
+    1: "causal drops the diagonal",
+    2: "sm_scale dropped",
+    3: "denominator starts at 1",
+    4: "row max dropped from lse",
+    5: "wrong row of V",
+    6: "strided instead of contiguous blocks",
+    7: "K and V swapped",
+    8: "log2 in lse",
+    9: "row max removed from the denominator only",
+    10: "last term of the dot product dropped",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=lambda m: MUTANTS[m].replace(" ", "_"))
+def test_planted_mistakes_are_caught(mutant):
+    attn = _attn_for(mutant)
+    caught = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(attn)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {mutant}: {MUTANTS[mutant]}"
+
+
+def test_page_fixture_matches_workload_table():
+    """The shared input module's copy of the page's test matrix agrees with
+    the cited fixture."""
+    import json
+    import os
+    from attn_inputs import PAGE_TEST_MATRIX
+    with open(os.path.join(os.path.dirname(__file__), "golden", "page_workloads.json")) as f:
+        fx = json.load(f)["fused_attention_test_matrix"]
+    names = {torch.float16: "fp16", torch.bfloat16: "bf16"}
+    assert [list(c[:4]) + [names[c[4]]] for c in PAGE_TEST_MATRIX] == fx["cases_Z_H_N_D_dtype"]
