@@ -1,0 +1,184 @@
+"""Python binding of the GB300 fused attention forward (``include/attn.h``).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library ``libattn_gb300.so`` (built in-tree by ``_build_ext.build()``).
+PyTorch supplies device memory and the current stream.  There is no CPU or
+PyTorch fallback: if the library is missing or a call fails, this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import _build_ext
+
+DENSE, CAUSAL, BLOCK_DIAG = 0, 1, 2
+F16, BF16 = 0, 1
+HEAD_DIMS = (64, 128, 256)
+
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_BLOCK_SIZE",
+          4: "ATTN_ERR_UNSUPPORTED", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_CUDA",
+          7: "ATTN_ERR_TIMEOUT", 8: "ATTN_ERR_ARG"}
+
+# Every function the C header declares, with its ctypes signature.
+_SIGNATURES = {
+    "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_work": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_double)] * 2),
+    "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_last_device_status": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                               ctypes.POINTER(ctypes.c_uint)]),
+    "attn_fwd_plan": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)] * 4),
+    "attn_abi_version": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build_ext.lib_path()
+    if not os.path.exists(p):
+        raise ImportError(f"CUDA library not built: {p} (run __graft_entry__.build() or "
+                          "attention_forward_15_gb300._build_ext.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float16:
+        return F16
+    if dt == torch.bfloat16:
+        return BF16
+    raise TypeError(f"q, k, v must be float16 or bfloat16, got {dt}")
+
+
+def work(B: int, H: int, L: int, D: int, mask_kind: int, block_size: int = 0,
+         dtype: torch.dtype = torch.float16) -> tuple[float, float]:
+    """(flops, bytes) of one forward: 4*D*attended pairs, and Q/K/V/O bytes."""
+    f, b = ctypes.c_double(), ctypes.c_double()
+    rc = load_library().attn_fwd_work(B, H, L, D, mask_kind, block_size, _dtype_code(dtype),
+                                      ctypes.byref(f), ctypes.byref(b))
+    if rc:
+        raise AttnError(rc, "attn_fwd_work")
+    return f.value, b.value
+
+
+def plan(B: int, H: int, L: int, D: int, mask_kind: int, block_size: int = 0,
+         dtype: torch.dtype = torch.float16, with_ctas: bool = True) -> dict:
+    u, c, t, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = load_library().attn_fwd_plan(B, H, L, D, mask_kind, block_size, _dtype_code(dtype),
+                                      ctypes.byref(u), ctypes.byref(c) if with_ctas else None,
+                                      ctypes.byref(t), ctypes.byref(s))
+    if rc:
+        raise AttnError(rc, "attn_fwd_plan")
+    out = {"units": u.value, "threads": t.value, "smem_bytes": s.value}
+    if with_ctas:
+        out["ctas"] = c.value
+    return out
+
+
+def last_device_status(device: int = 0) -> tuple[int, int]:
+    st, det = ctypes.c_int(), ctypes.c_uint()
+    rc = load_library().attn_last_device_status(device, ctypes.byref(st), ctypes.byref(det))
+    if rc:
+        raise AttnError(rc, "attn_last_device_status")
+    return st.value, det.value
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int = DENSE,
+        block_size: int = 0, sm_scale: float | None = None, return_lse: bool = True,
+        out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+        stream: torch.cuda.Stream | None = None):
+    """Fused attention forward of CUDA tensors q, k, v: [B, H, L, D], fp16/bf16.
+
+    Returns ``(o, lse)`` (``lse`` is None when ``return_lse`` is False); the
+    call is asynchronous on ``stream`` (default: the current stream).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, L, D]")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, L, D]")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must have the same shape")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if q.device != k.device or q.device != v.device:
+        raise ValueError("q, k and v must be on one device")
+    B, H, L, D = (int(x) for x in q.shape)
+    dt = _dtype_code(q.dtype)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty_like(q)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("out must be a contiguous tensor like q")
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, H, L), dtype=torch.float32,
+                                                              device=q.device)
+        if (tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32 or not lse.is_contiguous()
+                or lse.device != q.device):
+            raise ValueError("lse_out must be a contiguous float32 [B, H, L] tensor on q's device")
+    with torch.cuda.device(q.device):
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = load_library().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr() if lse is not None else None,
+                                     B, H, L, D, int(mask_kind), int(block_size), float(sm_scale),
+                                     dt, ctypes.c_void_p(s.cuda_stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int = DENSE,
+             block_size: int = 0, sm_scale: float | None = None, device: int = 0,
+             staging: dict | None = None):
+    """Forward of HOST tensors: copies q, k, v to the GPU, runs ``fwd`` and
+    copies o and lse back into host tensors (pinned when ``staging`` holds
+    them).  ``staging`` may hold preallocated device buffers ``q_d, k_d, v_d,
+    o_d, lse_d`` and host outputs ``o_h, lse_h`` to reuse across calls.
+    Returns ``(o_host, lse_host)`` after synchronising the stream."""
+    st = staging if staging is not None else {}
+    dev = torch.device("cuda", device)
+    names = ("q_d", "k_d", "v_d")
+    for name, t in zip(names, (q, k, v)):
+        if name not in st:
+            st[name] = torch.empty(t.shape, dtype=t.dtype, device=dev)
+        st[name].copy_(t, non_blocking=True)
+    o_d, lse_d = fwd(st["q_d"], st["k_d"], st["v_d"], mask_kind, block_size, sm_scale,
+                     out=st.get("o_d"), lse_out=st.get("lse_d"))
+    st["o_d"], st["lse_d"] = o_d, lse_d
+    if "o_h" not in st:
+        st["o_h"] = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
+        st["lse_h"] = torch.empty(lse_d.shape, dtype=lse_d.dtype, pin_memory=True)
+    st["o_h"].copy_(o_d, non_blocking=True)
+    st["lse_h"].copy_(lse_d, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return st["o_h"], st["lse_h"]

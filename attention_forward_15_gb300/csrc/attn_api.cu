@@ -1,0 +1,283 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// TMA tensor-map encoding, kernel selection and launch.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "attn.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+using attn::Cfg;
+using attn::FwdParams;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    unsigned int *status = nullptr;   // device status word written by timed-out waits
+    bool smem_attr[3][2] = {};        // per (head dim, dtype): dynamic smem attribute set
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int head_dim_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : (D == 256 ? 2 : -1)); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape/argument validation shared by every entry point (no CUDA calls).
+int validate_shape(int B, int H, int L, int D, int mask_kind, int block_size, int dtype) {
+    if (B < 0 || H < 0 || L < 0) return ATTN_ERR_SHAPE;
+    if (mask_kind < ATTN_MASK_DENSE || mask_kind > ATTN_MASK_BLOCK_DIAG) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (head_dim_index(D) < 0) return ATTN_ERR_UNSUPPORTED;
+    if (mask_kind == ATTN_MASK_BLOCK_DIAG) {
+        if (block_size <= 0) return ATTN_ERR_BLOCK_SIZE;
+        if (L > 0 && L % block_size != 0) return ATTN_ERR_BLOCK_SIZE;
+        if (!(block_size % attn::BN == 0 || attn::BN % block_size == 0)) return ATTN_ERR_UNSUPPORTED;
+    }
+    // element counts must stay addressable and TMA dimensions within 2^32
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+    const long long elems = bh * L * static_cast<long long>(D);
+    if (elems > (1LL << 46)) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
+struct Plan {
+    bool pair;
+    int n_qt, n_kv, n_units;
+};
+
+Plan make_plan(int B, int H, int L, int D) {
+    Plan pl;
+    pl.pair = D <= 128;
+    pl.n_qt = (L + attn::BM - 1) / attn::BM;
+    pl.n_kv = (L + attn::BN - 1) / attn::BN;
+    const int per_bh = pl.pair ? (pl.n_qt + 1) / 2 : pl.n_qt;
+    pl.n_units = B * H * per_bh;
+    return pl;
+}
+
+int threads_for(int D) { return D <= 128 ? Cfg<64, true>::THREADS : Cfg<256, false>::THREADS; }
+
+int smem_for(int D) {
+    switch (D) {
+        case 64: return Cfg<64, true>::SMEM_BYTES;
+        case 128: return Cfg<128, true>::SMEM_BYTES;
+        default: return Cfg<256, false>::SMEM_BYTES;
+    }
+}
+
+int load_encoder() {
+    if (g_encode) return ATTN_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return ATTN_OK;
+}
+
+// Per-device state: SM count and the status word (allocated once per device).
+int device_state(DeviceState **out, int *dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    int rc = load_encoder();
+    if (rc != ATTN_OK) return rc;
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        if (cudaMalloc(&st.status, sizeof(unsigned int)) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaMemset(st.status, 0, sizeof(unsigned int)) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+        st.ready = true;
+    }
+    *out = &st;
+    if (dev_out) *dev_out = dev;
+    return ATTN_OK;
+}
+
+// 3-D tensor map over a [BH, L, D] 16-bit array: box = 64 columns (128 bytes)
+// x 128 rows x 1 head, 128-byte swizzle; rows past L read as zero.
+int encode_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool BF16, bool PAIR>
+int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdParams prm, int dtype,
+           cudaStream_t stream) {
+    using C = Cfg<D, PAIR>;
+    auto kern = attn::attn_fwd_kernel<D, BF16, PAIR>;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        bool &set = st.smem_attr[head_dim_index(D)][BF16 ? 1 : 0];
+        if (!set) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM_BYTES) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            set = true;
+        }
+    }
+    CUtensorMap tq, tk, tv;
+    int rc = encode_map(&tq, q, prm.BH, prm.L, D, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tk, k, prm.BH, prm.L, D, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tv, v, prm.BH, prm.L, D, dtype);
+    if (rc != ATTN_OK) return rc;
+    const int grid = prm.n_units < st.sms ? prm.n_units : st.sms;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_abi_version(void) { return (1 << 16) | 0; }
+
+const char *attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_NULL: return "null pointer";
+        case ATTN_ERR_SHAPE: return "bad shape";
+        case ATTN_ERR_BLOCK_SIZE: return "block size must be positive and divide L";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported head dim, dtype, mask kind or block size";
+        case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+        case ATTN_ERR_ARG: return "bad argument";
+        default: return "unknown status";
+    }
+}
+
+int attn_fwd_work(int B, int H, int L, int D, int mask_kind, int block_size, int dtype,
+                  double *flops, double *bytes) {
+    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    if (rc != ATTN_OK) return rc;
+    const double bh = static_cast<double>(B) * H;
+    const double Ld = L;
+    double pairs;
+    if (mask_kind == ATTN_MASK_DENSE)
+        pairs = Ld * Ld;
+    else if (mask_kind == ATTN_MASK_CAUSAL)
+        pairs = Ld * (Ld + 1.0) / 2.0;
+    else
+        pairs = Ld * block_size;
+    if (flops) *flops = 4.0 * D * pairs * bh;
+    if (bytes) *bytes = 4.0 * bh * Ld * D * 2.0;
+    return ATTN_OK;
+}
+
+int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size, int dtype, int *units,
+                  int *ctas, int *threads, int *smem_bytes) {
+    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    if (rc != ATTN_OK) return rc;
+    const Plan pl = make_plan(B, H, L, D);
+    if (units) *units = pl.n_units;
+    if (threads) *threads = threads_for(D);
+    if (smem_bytes) *smem_bytes = smem_for(D);
+    if (ctas) {
+        int sms = 0, dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        *ctas = pl.n_units < sms ? pl.n_units : sms;
+    }
+    return ATTN_OK;
+}
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+             int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
+    if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
+    if (!q || !k || !v || !o) return ATTN_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 15u) != 0))
+        return ATTN_ERR_ALIGN;
+
+    DeviceState *st = nullptr;
+    rc = device_state(&st, nullptr);
+    if (rc != ATTN_OK) return rc;
+
+    const Plan pl = make_plan(B, H, L, D);
+    FwdParams prm;
+    prm.o = o;
+    prm.lse = lse;
+    prm.status = st->status;
+    prm.BH = B * H;
+    prm.L = L;
+    prm.mask = mask_kind;
+    prm.bs = mask_kind == ATTN_MASK_BLOCK_DIAG ? block_size : 0;
+    prm.n_qt = pl.n_qt;
+    prm.n_kv = pl.n_kv;
+    prm.n_units = pl.n_units;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bf16 = dtype == ATTN_BF16;
+    switch (D) {
+        case 64:
+            return bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
+                        : launch<64, false, true>(*st, q, k, v, prm, dtype, s);
+        case 128:
+            return bf16 ? launch<128, true, true>(*st, q, k, v, prm, dtype, s)
+                        : launch<128, false, true>(*st, q, k, v, prm, dtype, s);
+        default:
+            return bf16 ? launch<256, true, false>(*st, q, k, v, prm, dtype, s)
+                        : launch<256, false, false>(*st, q, k, v, prm, dtype, s);
+    }
+}
+
+int attn_last_device_status(int device, int *status, unsigned int *detail) {
+    if (!status) return ATTN_ERR_NULL;
+    if (device < 0 || device >= kMaxDevices) return ATTN_ERR_ARG;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned int word = 0;
+    int rc = ATTN_OK;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        DeviceState &st = g_dev[device];
+        if (st.ready) {
+            if (cudaDeviceSynchronize() != cudaSuccess ||
+                cudaMemcpy(&word, st.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+                cudaMemset(st.status, 0, sizeof word) != cudaSuccess)
+                rc = ATTN_ERR_CUDA;
+        }
+    }
+    cudaSetDevice(prev);
+    if (rc != ATTN_OK) return rc;
+    *status = (word & 0xffu) == attn::kStatusTimeout ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if (detail) *detail = word;
+    return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,667 @@
+// Fused attention forward for sm_103a (GB300): TMA -> shared memory ->
+// tcgen05.mma into tensor memory -> online softmax in registers -> tcgen05.mma
+// P.V back into tensor memory -> normalised output.
+//
+// What is computed (per query row i of head (b,h)):
+//   O_i   = sum_{j in A(i)} exp(s_ij - m_i) v_j / l_i,   s_ij = sm_scale q_i.k_j
+//   lse_i = m_i + ln l_i
+// with A(i) the attended keys of the mask kind (dense / causal j <= i /
+// block-diagonal floor(j/bs) == floor(i/bs)).  The key axis is walked tile by
+// tile with the online-softmax recurrence of the "Triton-CUDA Attention" page
+// (running max m, running denominator l, accumulator rescaled by
+// exp2(m_old - m_new)), in base 2 with sm_scale*log2(e) folded into one fma.
+//
+// Structure of one CTA (one CTA per SM, persistent over work units):
+//   * warp "TMA"     : one lane issues cp.async.bulk.tensor loads of Q tiles
+//                      into dedicated slots and of K/V tiles into a ring;
+//   * warp "MMA"     : one lane issues tcgen05.mma: S = Q K^T (both operands
+//                      K-major in shared memory, fp32 accumulator in TMEM) and
+//                      O += P V (P read from TMEM, V MN-major in shared memory);
+//                      it also owns the TMEM allocation;
+//   * softmax groups : 4 warps each, one thread per query row (= TMEM lane);
+//                      they read S from TMEM, apply the mask only on tiles
+//                      that cross it, run the online softmax, write P (16-bit)
+//                      over S in TMEM, rescale O in TMEM when the running max
+//                      grew past a threshold, and finally write O / l and lse.
+// Work is split into units; a unit is one head and one or two 128-row query
+// tiles ("lanes") that share the stream of K/V tiles.  Key tiles that lie
+// wholly outside a lane's attended range are never loaded or multiplied for it
+// (causal: tiles above the diagonal; block-diagonal: tiles of other blocks);
+// only tiles that cross the mask boundary go through the masked path.
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   pair mode (D <= 128): S/P lane 0 at col 0, S/P lane 1 at col 128,
+//                         O lane 0 at col 256, O lane 1 at col 256 + D;
+//   single mode (D = 256): one query tile, two S/P buffers at cols 0 and 128
+//                         (consecutive key tiles alternate), O at col 256.
+// P (16-bit, two per column) overwrites the first BN/2 columns of its S.
+//
+// Every mbarrier wait is bounded (about one second); on expiry the kernel
+// records a timeout in the status word, tells the other roles to stop through
+// a shared-memory flag, waits (bounded) for its own copies and MMAs in flight,
+// frees its tensor memory and returns.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int BM = 128;                       // query rows per tile (one per TMEM lane)
+constexpr int BN = 128;                       // keys per tile
+constexpr float kRescaleLog2 = 8.0f;          // rescale O only if the max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr unsigned kStatusTimeout = 7u;       // == ATTN_ERR_TIMEOUT
+
+enum : int { kMaskDense = 0, kMaskCausal = 1, kMaskBlock = 2 };
+
+struct FwdParams {
+    void *o;                 // [BH, L, D] 16-bit
+    float *lse;              // [BH, L] or nullptr
+    unsigned int *status;    // device status word
+    int BH, L, mask, bs;
+    int n_qt, n_kv;          // query / key tiles per head
+    int n_units;
+    float scale_log2;        // sm_scale * log2(e)
+};
+
+template <int D, bool PAIR>
+struct Cfg {
+    static constexpr int NQ = PAIR ? 2 : 1;           // query tiles resident per CTA
+    static constexpr int NWG = PAIR ? 2 : 1;          // softmax warpgroups
+    static constexpr int CHUNKS = D / 64;             // 128-byte-wide TMA boxes per row
+    static constexpr int CHUNK_BYTES = 128 * 128;     // one box: 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = 128 * D * 2;    // one Q, K or V tile
+    static constexpr int RING = D == 64 ? 8 : (D == 128 ? 5 : 2);
+    static constexpr int NUM_WARPS = 4 * NWG + 2;
+    static constexpr int THREADS = 32 * NUM_WARPS;
+    static constexpr int WARP_TMA = 4 * NWG;
+    static constexpr int WARP_MMA = 4 * NWG + 1;
+    // TMEM column of S/P buffer b and of the O accumulator of lane w
+    __device__ static constexpr uint32_t s_col(int b) { return static_cast<uint32_t>(b) * 128u; }
+    __device__ static constexpr uint32_t o_col(int w) {
+        return 256u + (PAIR ? static_cast<uint32_t>(w) * D : 0u);
+    }
+    static constexpr uint32_t TMEM_COLS = 512;
+    // shared memory (offsets from a 1024-byte aligned base)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_RING = NQ * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + RING * TILE_BYTES;
+    // barrier indices
+    static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4;
+    static constexpr int B_KVEMPTY = B_KVFULL + RING;
+    static constexpr int B_SFULL = B_KVEMPTY + RING;
+    static constexpr int B_PFULL = B_SFULL + 2;
+    static constexpr int B_ODONE = B_PFULL + 2;
+    static constexpr int B_DRAIN = B_ODONE + 2;
+    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // [0]: TMEM base, [1]: abort flag
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
+    static_assert(D == 64 || D == 128 || D == 256, "head dim");
+    static_assert(PAIR ? (2 * 128 + 2 * D <= 512) : (D == 256), "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// ------------------------------------------------------------ work units
+
+struct Unit {
+    int bh;
+    int qt[2];     // query tile of each lane, -1 if the lane is idle in this unit
+    int lo[2];     // key-tile range [lo, hi) of each lane
+    int hi[2];
+    int ulo, uhi;  // union of the lanes' ranges
+};
+
+// Key tiles a 128-row query tile attends (tiles wholly outside the mask are
+// excluded here, so they are never loaded or multiplied).
+__device__ __forceinline__ void kv_range(const FwdParams &p, int qt, int &lo, int &hi) {
+    if (p.mask == kMaskDense) {
+        lo = 0;
+        hi = p.n_kv;
+    } else if (p.mask == kMaskCausal) {
+        lo = 0;
+        hi = qt + 1;                          // BM == BN: the diagonal tile is qt
+    } else {
+        const int q0 = qt * BM;
+        const int q1 = min(q0 + BM, p.L);
+        const int klo = (q0 / p.bs) * p.bs;
+        const int khi = ((q1 - 1) / p.bs + 1) * p.bs;
+        lo = klo / BN;
+        hi = (khi + BN - 1) / BN;
+    }
+}
+
+// True if some (row, key) pair of the tile is outside the mask (or past L),
+// i.e. the tile needs the element-wise masked path.
+__device__ __forceinline__ bool tile_masked(const FwdParams &p, int qt, int j) {
+    if (p.mask == kMaskDense) return (j + 1) * BN > p.L;
+    if (p.mask == kMaskCausal) return j == qt;
+    return (p.bs % BN) != 0;
+}
+
+template <bool PAIR>
+__device__ __forceinline__ Unit make_unit(const FwdParams &p, int u) {
+    Unit U;
+    const int per_bh = PAIR ? (p.n_qt + 1) / 2 : p.n_qt;
+    int idx;
+    if (p.mask == kMaskCausal) {              // heaviest query tiles first
+        idx = per_bh - 1 - u / p.BH;
+        U.bh = u % p.BH;
+    } else {                                  // neighbouring units share a head
+        U.bh = u / per_bh;
+        idx = u % per_bh;
+    }
+    if (PAIR) {
+        U.qt[0] = 2 * idx;
+        U.qt[1] = (2 * idx + 1 < p.n_qt) ? 2 * idx + 1 : -1;
+    } else {
+        U.qt[0] = idx;
+        U.qt[1] = -1;
+    }
+    U.ulo = INT_MAX;
+    U.uhi = INT_MIN;
+    for (int w = 0; w < 2; ++w) {
+        if (U.qt[w] >= 0) {
+            kv_range(p, U.qt[w], U.lo[w], U.hi[w]);
+            U.ulo = min(U.ulo, U.lo[w]);
+            U.uhi = max(U.uhi, U.hi[w]);
+        } else {
+            U.lo[w] = U.hi[w] = 0;
+        }
+    }
+    return U;
+}
+
+__device__ __forceinline__ bool lane_uses(const Unit &U, int w, int j) {
+    return U.qt[w] >= 0 && j >= U.lo[w] && j < U.hi[w];
+}
+
+// Unit taken by CTA `cta` of `G` in round r (>= n_units means none).  Causal
+// units are sorted heaviest first and dealt in a snake order so that every
+// CTA gets a similar total.
+__device__ __forceinline__ int unit_of(const FwdParams &p, int cta, int G, int r) {
+    if (p.mask == kMaskCausal && (r & 1)) return r * G + (G - 1 - cta);
+    return r * G + cta;
+}
+
+// ------------------------------------------------------------ bounded waits
+
+struct Ctl {
+    volatile int *abort_flag;
+    unsigned int *status;
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site,
+                                       bool honour_abort) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (honour_abort && *c.abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicCAS(c.status, 0u, kStatusTimeout | (site << 8));
+                *c.abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, c, site, true);
+}
+
+// wait sites (recorded in the status word on a timeout)
+enum : unsigned {
+    kSiteQEmpty = 1, kSiteKvEmpty = 2, kSiteQFull = 3, kSiteKvFullK = 4, kSiteKvFullV = 5,
+    kSitePFull = 6, kSiteSFull = 7, kSiteODone = 8, kSiteDrain = 9
+};
+
+// ---------------------------------------------------------------- kernel
+
+template <int D, bool BF16, bool PAIR>
+__global__ void __launch_bounds__(Cfg<D, PAIR>::THREADS, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+    using C = Cfg<D, PAIR>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + C::OFF_BAR;
+    auto bar = [&](int idx) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(idx); };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    const Ctl ctl{reinterpret_cast<volatile int *>(misc + 1), p.status};
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const int cta = blockIdx.x;
+    const int rounds = (p.n_units + G - 1) / G;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL + 0), 1);
+        mbar_init(bar(C::B_QFULL + 1), 1);
+        mbar_init(bar(C::B_QEMPTY + 0), 1);
+        mbar_init(bar(C::B_QEMPTY + 1), 1);
+        for (int s = 0; s < C::RING; ++s) {
+            mbar_init(bar(C::B_KVFULL + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(C::B_SFULL + b), 1);
+            mbar_init(bar(C::B_PFULL + b), 4);   // one arrival per softmax warp
+            mbar_init(bar(C::B_ODONE + b), 1);
+        }
+        mbar_init(bar(C::B_DRAIN), 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::WARP_TMA && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+    }
+    if (warp == C::WARP_MMA) {
+        tmem_alloc(s_base + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == C::WARP_TMA) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            uint32_t rc = 0;             // K/V ring position
+            uint32_t qn[2] = {0, 0};     // Q loads issued per slot
+            bool ok = true;
+            for (int r = 0; r < rounds && ok; ++r) {
+                const int u = unit_of(p, cta, G, r);
+                if (u >= p.n_units) continue;
+                const Unit U = make_unit<PAIR>(p, u);
+                for (int w = 0; w < C::NQ && ok; ++w) {
+                    if (U.qt[w] < 0) continue;
+                    ok = wait_bar(bar(C::B_QEMPTY + w), (qn[w] & 1u) ^ 1u, ctl, kSiteQEmpty);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::B_QFULL + w), C::TILE_BYTES);
+                    const uint32_t dst = s_base + C::OFF_Q + w * C::TILE_BYTES;
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d(dst + c * C::CHUNK_BYTES, &tmap_q, c * 64, U.qt[w] * BM, U.bh,
+                                    bar(C::B_QFULL + w));
+                    ++qn[w];
+                }
+                for (int j = U.ulo; j < U.uhi && ok; ++j) {
+                    if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
+                    for (int kind = 0; kind < 2 && ok; ++kind) {
+                        const uint32_t slot = rc % C::RING;
+                        ok = wait_bar(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u, ctl,
+                                      kSiteKvEmpty);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::TILE_BYTES);
+                        const uint32_t dst = s_base + C::OFF_RING + slot * C::TILE_BYTES;
+                        const CUtensorMap *m = kind == 0 ? &tmap_k : &tmap_v;
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_load_3d(dst + c * C::CHUNK_BYTES, m, c * 64, j * BN, U.bh,
+                                        bar(C::B_KVFULL + slot));
+                        ++rc;
+                    }
+                }
+            }
+            if (*ctl.abort_flag) {
+                // Stopping early: let the copies already issued land before the
+                // CTA's shared memory goes away.
+                const uint32_t first = rc > static_cast<uint32_t>(C::RING) ? rc - C::RING : 0u;
+                for (uint32_t i = first; i < rc; ++i)
+                    wait_slow(bar(C::B_KVFULL + i % C::RING), (i / C::RING) & 1u, ctl, kSiteDrain, false);
+                for (int w = 0; w < C::NQ; ++w)
+                    if (qn[w] > 0)
+                        wait_slow(bar(C::B_QFULL + w), (qn[w] - 1) & 1u, ctl, kSiteDrain, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
+            constexpr uint32_t IDESC_PV = idesc_f16_f32acc(BF16, BM, D, true);
+            const uint32_t q_smem = s_base + C::OFF_Q;
+            const uint32_t ring_smem = s_base + C::OFF_RING;
+            // S = Q K^T: k-step kk covers head-dim columns [16kk, 16kk+16): box kk/4,
+            // 32-byte offset (kk%4) inside the 128-byte swizzled row.
+            auto qk_desc = [&](uint32_t base, int kk) -> uint64_t {
+                return sdesc_sw128(base + (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32, 16, 1024);
+            };
+            // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
+            // consecutive 64-column boxes of V are C::CHUNK_BYTES apart.
+            auto v_desc = [&](uint32_t base, int kk) -> uint64_t {
+                return sdesc_sw128(base + kk * 16 * 128, C::CHUNK_BYTES, 1024);
+            };
+            auto issue_s = [&](int w, int sbuf, uint32_t kslot) {
+                const uint32_t qb = q_smem + w * C::TILE_BYTES;
+                const uint32_t kb = ring_smem + kslot * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::s_col(sbuf), qk_desc(qb, kk), qk_desc(kb, kk), IDESC_S, kk > 0);
+            };
+            auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
+                const uint32_t vb = ring_smem + vslot * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + C::o_col(ocol_idx), tmem + C::s_col(sbuf) + kk * 8, v_desc(vb, kk),
+                           IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+            };
+
+            uint32_t rc = 0;
+            uint32_t qn[2] = {0, 0};
+            uint32_t pn[2] = {0, 0};     // P-ready waits per S buffer
+            bool ok = true;
+            for (int r = 0; r < rounds && ok; ++r) {
+                const int u = unit_of(p, cta, G, r);
+                if (u >= p.n_units) continue;
+                const Unit U = make_unit<PAIR>(p, u);
+                for (int w = 0; w < C::NQ && ok; ++w) {
+                    if (U.qt[w] < 0) continue;
+                    ok = wait_bar(bar(C::B_QFULL + w), qn[w] & 1u, ctl, kSiteQFull);
+                    ++qn[w];
+                }
+                if (!ok) break;
+                tc_fence_after();
+                if constexpr (PAIR) {
+                    int pend_j[2] = {-1, -1};
+                    uint32_t pend_v[2] = {0, 0};
+                    int npv[2] = {0, 0};
+                    auto flush_pv = [&](int w) -> bool {
+                        if (!wait_bar(bar(C::B_PFULL + w), pn[w] & 1u, ctl, kSitePFull)) return false;
+                        ++pn[w];
+                        const uint32_t vslot = pend_v[w] % C::RING;
+                        if (!wait_bar(bar(C::B_KVFULL + vslot), (pend_v[w] / C::RING) & 1u, ctl,
+                                      kSiteKvFullV))
+                            return false;
+                        tc_fence_after();
+                        issue_pv(w, w, vslot, npv[w] > 0);
+                        ++npv[w];
+                        mma_commit(bar(C::B_ODONE + w));
+                        const bool other_needs = pend_j[1 - w] == pend_j[w];
+                        pend_j[w] = -1;
+                        if (!other_needs) mma_commit(bar(C::B_KVEMPTY + vslot));
+                        return true;
+                    };
+                    for (int j = U.ulo; j < U.uhi && ok; ++j) {
+                        const bool use0 = lane_uses(U, 0, j), use1 = lane_uses(U, 1, j);
+                        if (!use0 && !use1) continue;
+                        const uint32_t kpos = rc, vpos = rc + 1;
+                        rc += 2;
+                        const uint32_t kslot = kpos % C::RING;
+                        ok = wait_bar(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u, ctl,
+                                      kSiteKvFullK);
+                        if (!ok) break;
+                        tc_fence_after();
+                        for (int w = 0; w < 2 && ok; ++w) {
+                            if (!(w == 0 ? use0 : use1)) continue;
+                            if (pend_j[w] >= 0) ok = flush_pv(w);
+                            if (!ok) break;
+                            issue_s(w, w, kslot);
+                            mma_commit(bar(C::B_SFULL + w));
+                            if (j == U.hi[w] - 1) mma_commit(bar(C::B_QEMPTY + w));
+                            pend_j[w] = j;
+                            pend_v[w] = vpos;
+                        }
+                        if (ok) mma_commit(bar(C::B_KVEMPTY + kslot));
+                    }
+                    for (int w = 0; w < 2 && ok; ++w)
+                        if (pend_j[w] >= 0) ok = flush_pv(w);
+                } else {
+                    // One query tile, S buffers alternate: S(0), S(1), PV(0), S(2), PV(1), ...
+                    const int n = U.hi[0] - U.lo[0];
+                    const uint32_t base = rc;
+                    rc += 2u * static_cast<uint32_t>(n);
+                    auto do_s = [&](int t) -> bool {
+                        const uint32_t kpos = base + 2u * t;
+                        const uint32_t kslot = kpos % C::RING;
+                        if (!wait_bar(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u, ctl,
+                                      kSiteKvFullK))
+                            return false;
+                        tc_fence_after();
+                        issue_s(0, t & 1, kslot);
+                        mma_commit(bar(C::B_SFULL + (t & 1)));
+                        mma_commit(bar(C::B_KVEMPTY + kslot));
+                        if (t == n - 1) mma_commit(bar(C::B_QEMPTY + 0));
+                        return true;
+                    };
+                    ok = do_s(0);
+                    for (int t = 0; t < n && ok; ++t) {
+                        if (t + 1 < n) ok = do_s(t + 1);
+                        if (!ok) break;
+                        const int b = t & 1;
+                        ok = wait_bar(bar(C::B_PFULL + b), pn[b] & 1u, ctl, kSitePFull);
+                        if (!ok) break;
+                        ++pn[b];
+                        const uint32_t vpos = base + 2u * t + 1u;
+                        const uint32_t vslot = vpos % C::RING;
+                        ok = wait_bar(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u, ctl,
+                                      kSiteKvFullV);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(b, 0, vslot, t > 0);
+                        mma_commit(bar(C::B_ODONE + b));
+                        mma_commit(bar(C::B_KVEMPTY + vslot));
+                    }
+                }
+            }
+            // Every MMA (and the barrier arrivals its commits make) must be done
+            // before the CTA frees its tensor memory and exits.
+            mma_commit(bar(C::B_DRAIN));
+            wait_slow(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax groups
+        const int wg = warp >> 2;                       // lane (query tile slot) of this group
+        const int wq = warp & 3;                        // TMEM lane quarter of this warp
+        const int row = wq * 32 + lane;                 // query row inside the tile
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const float sc = p.scale_log2;
+        const float fill = sc >= 0.f ? -INFINITY : INFINITY;
+        uint32_t sn[2] = {0, 0};      // S-ready waits per buffer
+        uint32_t made[2] = {0, 0};    // P tiles handed to the MMA warp per buffer
+        uint32_t seen[2] = {0, 0};    // P.V completions confirmed per buffer
+        bool ok = true;
+
+        // All 32 lanes poll; the outcome is made warp-uniform so that the
+        // warp-collective tcgen05 instructions after a wait never diverge.
+        auto wait_warp = [&](uint32_t bar_addr, uint32_t parity, unsigned site) -> bool {
+            const bool r = wait_bar(bar_addr, parity, ctl, site);
+            return __all_sync(0xffffffffu, r);
+        };
+        auto wait_pv = [&](int b) -> bool {
+            if (seen[b] < made[b]) {
+                if (!wait_warp(bar(C::B_ODONE + b), (made[b] - 1) & 1u, kSiteODone)) return false;
+                seen[b] = made[b];
+            }
+            return true;
+        };
+
+        for (int r = 0; r < rounds && ok; ++r) {
+            const int u = unit_of(p, cta, G, r);
+            if (u >= p.n_units) continue;
+            const Unit U = make_unit<PAIR>(p, u);
+            const int qt = U.qt[wg];
+            if (qt < 0) continue;
+            const int i = qt * BM + row;                // query row in the head
+            const bool row_valid = i < p.L;
+            // attended keys of row i: [klo, khi)
+            int klo, khi;
+            if (p.mask == kMaskDense) {
+                klo = 0;
+                khi = p.L;
+            } else if (p.mask == kMaskCausal) {
+                klo = 0;
+                khi = i + 1;
+            } else {
+                klo = (i / p.bs) * p.bs;
+                khi = klo + p.bs;
+            }
+            float m_ref = -INFINITY;                    // running max (log2 units, may lag)
+            float l = 0.f;                              // running denominator
+            int t = 0;
+            for (int j = U.lo[wg]; j < U.hi[wg] && ok; ++j, ++t) {
+                const int b = PAIR ? wg : (t & 1);
+                ok = wait_warp(bar(C::B_SFULL + b), sn[b] & 1u, kSiteSFull);
+                if (!ok) break;
+                ++sn[b];
+                tc_fence_after();
+                const uint32_t s_addr = tmem + lane_off + C::s_col(b);
+                float s[BN];
+                {
+                    uint32_t raw[BN];
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+                        tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(raw[c]);
+                }
+                const bool masked = tile_masked(p, qt, j);
+                const int rel_lo = klo - j * BN, rel_hi = khi - j * BN;
+                if (masked) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c < rel_lo || c >= rel_hi) s[c] = fill;
+                }
+                // row extreme of the raw scores (max for sm_scale >= 0, else min)
+                float ext[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ext[e] = s[e];
+                if (sc >= 0.f) {
+#pragma unroll
+                    for (int c = 8; c < BN; ++c) ext[c & 7] = fmaxf(ext[c & 7], s[c]);
+#pragma unroll
+                    for (int e = 4; e > 0; e >>= 1)
+#pragma unroll
+                        for (int f = 0; f < e; ++f) ext[f] = fmaxf(ext[f], ext[f + e]);
+                } else {
+#pragma unroll
+                    for (int c = 8; c < BN; ++c) ext[c & 7] = fminf(ext[c & 7], s[c]);
+#pragma unroll
+                    for (int e = 4; e > 0; e >>= 1)
+#pragma unroll
+                        for (int f = 0; f < e; ++f) ext[f] = fminf(ext[f], ext[f + e]);
+                }
+                const float m_tile = isinf(ext[0]) ? -INFINITY : ext[0] * sc;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (t == 0) {
+                    m_ref = m_tile;
+                } else if (m_tile > m_ref + kRescaleLog2) {
+                    alpha = ex2_approx(m_ref - m_tile);
+                    m_ref = m_tile;
+                    rescale = true;
+                }
+                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                float part[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[e] = 0.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int c0 = 64 * h + 2 * e;
+                        float p0 = ex2_approx(fmaf(s[c0], sc, neg_m));
+                        float p1 = ex2_approx(fmaf(s[c0 + 1], sc, neg_m));
+                        if (masked) {
+                            if (c0 < rel_lo || c0 >= rel_hi) p0 = 0.f;
+                            if (c0 + 1 < rel_lo || c0 + 1 >= rel_hi) p1 = 0.f;
+                        }
+                        part[(2 * e) & 7] += p0;
+                        part[(2 * e + 1) & 7] += p1;
+                        pk[e] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st32(s_addr + 32 * h, pk);
+                }
+#pragma unroll
+                for (int e = 4; e > 0; e >>= 1)
+#pragma unroll
+                    for (int f = 0; f < e; ++f) part[f] += part[f + e];
+                l = l * alpha + part[0];
+
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O must hold every earlier P.V before it is rescaled.  In pair
+                    // mode the S-ready commit already covered it; in single mode
+                    // the previous tile's P.V used the other buffer.
+                    if (!PAIR) ok = wait_pv(b ^ 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t o_addr = tmem + lane_off + C::o_col(PAIR ? wg : 0);
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(o_addr + 32 * c, raw);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            raw[e] = __float_as_uint(__uint_as_float(raw[e]) * alpha);
+                        tmem_st32(o_addr + 32 * c, raw);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
+                ++made[b];
+            }
+            if (!ok) break;
+            // ------------------------------------------------ epilogue: O / l, lse
+            if (PAIR) {
+                ok = wait_pv(wg);
+            } else {
+                ok = wait_pv(0) && wait_pv(1);
+            }
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            const uint32_t o_addr = tmem + lane_off + C::o_col(PAIR ? wg : 0);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
+                                                   ((static_cast<size_t>(U.bh) * p.L + i) * D) * 2);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(o_addr + 32 * c, raw);
+                tmem_wait_ld();
+                uint32_t w16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * inv_l,
+                                         __uint_as_float(raw[2 * e + 1]) * inv_l);
+                if (row_valid) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
+                                                     w16[4 * v4 + 3]);
+                }
+            }
+            if (row_valid && p.lse != nullptr) {
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                p.lse[static_cast<size_t>(U.bh) * p.L + i] =
+                    (m_use + lg2_approx(l)) * 0.69314718055994530942f;
+            }
+            tc_fence_before();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace attn

@@ -1,0 +1,443 @@
+"""Benchmark of the GB300 fused attention forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-all]
+
+One step = one fused attention forward (every step of the path runs in the
+CUDA library) over one batch of the workload's synthetic inputs.  The headline
+workload is the dense fp16 attention B=4, H=16, L=1024, D=64 (with lse).
+Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU (the forward needs no exchange between
+GPUs), ranks meet at a barrier around the timed region and the slowest rank's
+time is reported; ``value`` is the work of all ranks over that time.
+
+``--impl reference`` times the CPU fp64 oracle instead (the slow program the
+library is checked against) on the host cores, one head of the workload per
+step; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from attn_inputs import HEADLINE, MASK_NAMES, WORKLOADS, make_workload_inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "attention fwd TFLOP/s (unmasked FLOPs) and % of roofline per mask kind, 1×GB300"
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh", "attn_api.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-all", action="store_true",
+                    help="skip the per-mask-kind measurements of the other workloads")
+    ap.add_argument("--soak-s", type=float, default=2.0,
+                    help="seconds of untimed launches before the timed region (clock sampling)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "attention_forward_15_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_sources_sha256_16") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+
+def rotation_sets(w, dev, nbytes_set):
+    """Enough copies of the inputs/outputs that one pass over them exceeds
+    twice the L2, so consecutive steps read their inputs from HBM."""
+    return max(2, math.ceil(2 * L2_BYTES / nbytes_set))
+
+
+def make_device_inputs(w, dev):
+    if w.name == HEADLINE:
+        return tuple(t.to(dev) for t in make_workload_inputs(w))   # the seeded CPU recipe
+    # same distribution, drawn on the device (faster for the large workloads)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.L, w.D)
+    return tuple(torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+                 .mul_(w.std).to(w.dtype) for _ in range(3))
+
+
+def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None):
+    """Device time per step (ms) of the forward on workload w.
+
+    Steps rotate over enough input/output sets that each step reads its
+    inputs from HBM, and are replayed from CUDA graphs (the launch loop is
+    captured once: per-call host work such as tensor-map encoding is not in
+    the timed region, only the kernels).  Returns (ms_per_step, info)."""
+    q, k, v = make_device_inputs(w, dev)
+    per_set = 4 * q.numel() * q.element_size() + w.B * w.H * w.L * 4
+    nsets = rotation_sets(w, dev, per_set)
+    sets = []
+    for s in range(nsets):
+        qs, ks, vs = (q, k, v) if s == 0 else (q.clone(), k.clone(), v.clone())
+        sets.append((qs, ks, vs, torch.empty_like(q),
+                     torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)))
+
+    def step(i):
+        qs, ks, vs, o, lse = sets[i % nsets]
+        af.fwd(qs, ks, vs, w.mask, w.block_size, w.sm_scale, out=o, lse_out=lse)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for i in range(max(warmup, 1)):
+            step(i)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+
+    chunk = min(steps, max(nsets, 1000 // nsets * nsets))
+    graphs = []
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(i)
+        return g
+    full = capture(chunk)
+    rem = steps % chunk
+    tail = capture(rem) if rem else None
+    torch.cuda.synchronize(dev)
+    replays = steps // chunk
+
+    def run_timed_region():
+        for _ in range(replays):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+
+    if soak_s > 0:
+        if sampler:
+            sampler.start()
+        t_end = time.perf_counter() + soak_s
+        while time.perf_counter() < t_end:
+            full.replay()
+            torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run_timed_region()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / steps
+    st, det = af.last_device_status(dev.index)
+    if st != 0:
+        raise RuntimeError(f"device status {st} (detail {det:#x}) after the timed region")
+    del graphs
+    return ms, {"rotating_sets": nsets, "set_bytes": per_set, "graph_launches": chunk}
+
+
+def time_e2e(af, w, dev, steps, warmup):
+    """End to end through the public host API: each step copies q, k, v from
+    pinned host memory, runs the forward and copies o and lse back."""
+    q, k, v = (t.pin_memory() for t in make_workload_inputs(w)) if w.name == HEADLINE else \
+        (t.cpu().pin_memory() for t in make_device_inputs(w, dev))
+    staging: dict = {}
+    for _ in range(max(warmup, 1)):
+        af.fwd_host(q, k, v, w.mask, w.block_size, w.sm_scale, device=dev.index, staging=staging)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        af.fwd_host(q, k, v, w.mask, w.block_size, w.sm_scale, device=dev.index, staging=staging)
+    dt = (time.perf_counter() - t0) / steps
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = staging["o_h"].numel() * staging["o_h"].element_size() + staging["lse_h"].numel() * 4
+    return dt, h2d, d2h
+
+
+# ----------------------------------------------------------------- oracle (CPU)
+
+def oracle_sample(w, n_heads: int):
+    """Time the CPU fp64 oracle on the first n_heads (b, h) heads of workload
+    w (all rows of each); returns (seconds, flops of the sample, threads)."""
+    import oracle
+    q, k, v = make_workload_inputs(w)
+    BH = w.B * w.H
+    n_heads = max(1, min(n_heads, BH))
+    qf, kf, vf = (t.reshape(BH, 1, w.L, w.D)[:n_heads].contiguous() for t in (q, k, v))
+    threads = os.cpu_count() or 1
+    oracle.load()
+    t0 = time.perf_counter()
+    oracle.attention(qf, kf, vf, w.mask, w.block_size, w.sm_scale, nthreads=threads)
+    dt = time.perf_counter() - t0
+    import attention_forward_15_gb300 as af
+    flops, _ = af.work(1, n_heads, w.L, w.D, w.mask, w.block_size, w.dtype)
+    return dt, flops, threads
+
+
+def cpu_baseline(w, target_s: float = 10.0):
+    """Oracle throughput on the host cores on a bounded sample of workload w
+    (calibrated on one head, then enough heads for about target_s seconds)."""
+    dt1, f1, threads = oracle_sample(w, 1)
+    n = max(1, min(w.B * w.H, int(target_s / max(dt1, 1e-3))))
+    if n > 1:
+        dt, f, threads = oracle_sample(w, n)
+    else:
+        dt, f = dt1, f1
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"all {w.L} rows of {n} of the {w.B * w.H} (b,h) heads, fp64, "
+                      f"{dt:.2f} s wall"}
+
+
+# ----------------------------------------------------------------- main
+
+def roofline_for(w, flops, nbytes, ms, peaks, peaks_kind, traffic):
+    t = ms * 1e-3
+    tc = peaks["bf16_tflops"]            # fp16 and bf16 have the same dense tensor rate
+    bw = peaks["hbm_gbs"]
+    t_tensor = flops / (tc * 1e12)
+    t_hbm = nbytes / (bw * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flops / t / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc, "unit": "TFLOP/s",
+                "frac": round(achieved / tc, 4), "traffic": traffic,
+                "peak_source": f"{peaks_kind} bf16_tflops (burst; fp16 rate equal)"}
+    achieved = nbytes / t / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": bw, "unit": "GB/s",
+            "frac": round(achieved / bw, 4), "traffic": traffic,
+            "peak_source": f"{peaks_kind} hbm_gbs"}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, w, world)
+        return
+
+    import attention_forward_15_gb300 as af
+    from attention_forward_15_gb300 import _build_ext
+    if not os.path.exists(_build_ext.lib_path()):
+        _build_ext.build()
+    af.load_library()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA library has no CPU path)")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+        dist = tdist
+
+    peaks, peaks_kind = load_peaks()
+    flops, nbytes = af.work(w.B, w.H, w.L, w.D, w.mask, w.block_size, w.dtype)
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    ms, info = time_workload(af, w, dev, args.steps, args.warmup, soak_s=args.soak_s,
+                             sampler=sampler, dist=dist)
+    clocks = sampler.stop() if sampler else None
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    e2e_s, h2d, d2h = time_e2e(af, w, dev, max(10, min(args.steps, 200)), 3)
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    per_mask = {}
+    if not args.no_all:
+        for name, ow in WORKLOADS.items():
+            if name == w.name:
+                continue
+            f2, b2 = af.work(ow.B, ow.H, ow.L, ow.D, ow.mask, ow.block_size, ow.dtype)
+            steps2 = max(5, min(args.steps, int(2e12 / f2) + 5, 200))
+            ms2, _ = time_workload(af, ow, dev, steps2, 3)
+            rl = roofline_for(ow, f2, b2, ms2, peaks, peaks_kind, ncu_traffic(name))
+            per_mask[name] = {"mask": MASK_NAMES[ow.mask], "ms": round(ms2, 4),
+                              "tflops": round(f2 / (ms2 * 1e-3) / 1e12, 2),
+                              "roofline_bound": rl["bound"], "roofline_frac": rl["frac"],
+                              "achieved": rl["achieved"], "unit": rl["unit"]}
+    if dist:
+        dist.barrier()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    value = flops * world / (ms * 1e-3) / 1e12
+    cfg = w.describe()
+    cfg.update({"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "l2": f"{info['rotating_sets']} rotating input/output sets of "
+                      f"{info['set_bytes'] / 2**20:.1f} MiB (> 2x the 129 MB L2)",
+                "launch": f"CUDA graph replay of {info['graph_launches']} launches",
+                "flops_per_step": flops, "bytes_per_step": nbytes,
+                "clocks_note": f"sampled over a {args.soak_s:.1f} s soak of the same graph "
+                               "immediately before the timed region"})
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if w.dtype == torch.float16 else "bf16", "data": "synthetic",
+        "config": cfg,
+        "roofline": roofline_for(w, flops, nbytes, ms, peaks, peaks_kind, ncu_traffic(w.name)),
+        "e2e": {"value": round(flops * world / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "per_workload": per_mask or None,
+    }
+    out["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args, w, world):
+    """The oracle as the reference arm: each step computes one (b,h) head of
+    the workload in fp64 on the host cores."""
+    import oracle
+    import attention_forward_15_gb300 as af   # for the work count only (host function)
+    q, k, v = make_workload_inputs(w)
+    BH = w.B * w.H
+    threads = os.cpu_count() or 1
+    oracle.load()
+    heads = [t.reshape(BH, 1, w.L, w.D) for t in (q, k, v)]
+
+    def step(i):
+        h = i % BH
+        oracle.attention(heads[0][h:h + 1], heads[1][h:h + 1], heads[2][h:h + 1], w.mask,
+                         w.block_size, w.sm_scale, nthreads=threads)
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = (time.perf_counter() - t0) / args.steps
+    f_head, _ = af.work(1, 1, w.L, w.D, w.mask, w.block_size, w.dtype)
+    value = f_head / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": w.describe(),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"one (b,h) head of {BH} per step, all {w.L} rows, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

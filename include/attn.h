@@ -1,0 +1,124 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * The operation (one call):
+ *
+ *     O   = softmax(Q K^T * sm_scale + mask) V
+ *     lse = log(sum_j exp(sm_scale * q_i . k_j))   over the attended keys j
+ *
+ * over Q, K, V of shape [B, H, L, D].  The masks are the three the source
+ * pages define:
+ *   ATTN_MASK_DENSE       every key is attended (the "Triton-CUDA Attention"
+ *                         page, standard Flash Attention example);
+ *   ATTN_MASK_CAUSAL      key j is attended by query i iff j <= i (the
+ *                         "Fused Attention" page, stage-2 mask, top-left
+ *                         aligned, L_q = L_k);
+ *   ATTN_MASK_BLOCK_DIAG  key j is attended by query i iff floor(j/bs) ==
+ *                         floor(i/bs): only the diagonal bs x bs blocks of the
+ *                         L x L attention matrix take part (the "TLX Block
+ *                         Attention" page, block-diagonal definition).
+ * The computation is tiled with the online-softmax recurrence (the
+ * "Triton-CUDA Attention" page, online softmax section), so the L x L matrix
+ * is never written to memory.  lse is the natural-log log-sum-exp of the
+ * scaled scores (the "Fused Attention" page, epilogue m_i += log(l_i)).
+ *
+ * Layout: q, k, v and o are contiguous row-major [B, H, L, D] arrays of the
+ * element type `dtype` (fp16 or bf16), D innermost; lse is a contiguous fp32
+ * [B, H, L] array.  All five pointers are DEVICE pointers on the current CUDA
+ * device, each 16-byte aligned.  The caller owns every buffer; the library
+ * never allocates, frees or retains them.
+ */
+#ifndef ATTN_FWD_GB300_ATTN_H
+#define ATTN_FWD_GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_MASK_DENSE = 0,
+    ATTN_MASK_CAUSAL = 1,
+    ATTN_MASK_BLOCK_DIAG = 2
+} attn_mask_kind;
+
+typedef enum {
+    ATTN_F16 = 0,
+    ATTN_BF16 = 1
+} attn_dtype;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,          /* a required pointer is NULL                        */
+    ATTN_ERR_SHAPE = 2,         /* B, H or L negative, or a size overflows           */
+    ATTN_ERR_BLOCK_SIZE = 3,    /* block-diagonal: bs <= 0 or bs does not divide L   */
+    ATTN_ERR_UNSUPPORTED = 4,   /* head_dim, dtype, mask kind or bs not supported    */
+    ATTN_ERR_ALIGN = 5,         /* a pointer is not 16-byte aligned                  */
+    ATTN_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed                 */
+    ATTN_ERR_TIMEOUT = 7,       /* a device-side pipeline wait ran out (see below)   */
+    ATTN_ERR_ARG = 8            /* sm_scale not finite, or another bad argument      */
+} attn_status;
+
+/*
+ * attn_fwd -- enqueue one fused attention forward on `stream`.
+ *
+ *   q, k, v     inputs, [B, H, L, D] of `dtype`, device memory, read only.
+ *   o           output, [B, H, L, D] of `dtype`, device memory, fully written.
+ *   lse         output, [B, H, L] fp32, device memory; may be NULL (not written).
+ *   B, H, L     batch, heads, sequence length (queries = keys = L).  A zero
+ *               size is an empty problem: ATTN_OK, nothing is launched.
+ *   D           head dim: 64, 128 or 256.
+ *   mask_kind   an attn_mask_kind.
+ *   block_size  the block size bs of ATTN_MASK_BLOCK_DIAG (ignored otherwise);
+ *               bs must divide L and be a divisor or a multiple of 128.
+ *   sm_scale    the score scale (the pages use 1/sqrt(D)); any finite value.
+ *   dtype       an attn_dtype.
+ *   stream      a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Returns ATTN_OK once the kernel is enqueued; the outputs are valid after
+ * the stream is synchronised.  Argument errors are detected on the host
+ * before any CUDA call and nothing is launched or written.  A failed launch
+ * returns ATTN_ERR_CUDA.  Every wait inside the kernel is bounded (about one
+ * second); if one runs out the kernel stops, frees its tensor memory and
+ * records ATTN_ERR_TIMEOUT in a per-device status word that
+ * attn_last_device_status() reads.  Reentrant; safe from several host threads.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int L, int D, int mask_kind, int block_size,
+             float sm_scale, int dtype, void *stream);
+
+/*
+ * attn_fwd_work -- the algorithmic work of one attn_fwd call, for throughput
+ * and roofline figures.  flops = 4 * D * (attended (i, j) pairs summed over
+ * B*H heads): two flops per multiply-add, for both Q K^T and P V; masked pairs
+ * are not counted.  bytes = Q, K and V read once plus O written once
+ * (4 * B*H*L*D * element size); lse bytes are not counted.  Either output
+ * pointer may be NULL.  Returns an attn_status (same validation as attn_fwd).
+ */
+int attn_fwd_work(int B, int H, int L, int D, int mask_kind, int block_size,
+                  int dtype, double *flops, double *bytes);
+
+/* Human-readable name of an attn_status (static storage; never NULL). */
+const char *attn_status_string(int status);
+
+/*
+ * attn_last_device_status -- read and clear the device status word of CUDA
+ * device `device` (the word in-kernel timeouts write).  Synchronises that
+ * device first.  *status receives ATTN_OK or ATTN_ERR_TIMEOUT; *detail (may
+ * be NULL) receives the raw word (role and wait site of the first timeout).
+ * Returns an attn_status for the query itself.
+ */
+int attn_last_device_status(int device, int *status, unsigned int *detail);
+
+/* Number of work units and CTAs attn_fwd would launch for these arguments on
+ * the current device (for tests and reports); returns an attn_status. */
+int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size,
+                  int dtype, int *units, int *ctas, int *threads, int *smem_bytes);
+
+/* ABI version of this header: (major << 16) | minor. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_GB300_ATTN_H */

@@ -1,0 +1,91 @@
+"""CPU-only checks of the C ABI: the library loads without a GPU, exports every
+function include/attn.h declares, and rejects bad arguments on the host before
+any CUDA call.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_15_gb300 import _build_ext
+    import attention_forward_15_gb300 as af
+    _build_ext.build()
+    return af.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for n in ("attn_fwd", "attn_fwd_work", "attn_status_string", "attn_last_device_status"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared in attn.h but not exported"
+
+
+def test_abi_version(lib):
+    assert lib.attn_abi_version() >> 16 == 1
+
+
+def test_status_strings(lib):
+    for s in range(0, 9):
+        assert lib.attn_status_string(s)
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+def _fwd(lib, B=1, H=1, L=256, D=128, mask=0, bs=0, scale=0.1, dtype=0, ptrs=(16, 16, 16, 16), lse=None):
+    q, k, v, o = (ctypes.c_void_p(p) if p else None for p in ptrs)
+    return lib.attn_fwd(q, k, v, o, lse, B, H, L, D, mask, bs, scale, dtype, None)
+
+
+def test_host_validation_before_any_cuda_call(lib):
+    # every case is rejected on the host: no device is touched
+    assert _fwd(lib, D=96) == 4
+    assert _fwd(lib, D=32) == 4
+    assert _fwd(lib, dtype=2) == 4
+    assert _fwd(lib, mask=3) == 4
+    assert _fwd(lib, B=-1) == 2
+    assert _fwd(lib, L=-5) == 2
+    assert _fwd(lib, mask=2, bs=0) == 3
+    assert _fwd(lib, mask=2, bs=48) == 3          # 48 does not divide 256
+    assert _fwd(lib, mask=2, bs=96, L=384) == 4   # neither a divisor nor a multiple of 128
+    assert _fwd(lib, scale=float("nan")) == 8
+    assert _fwd(lib, scale=float("inf")) == 8
+    assert _fwd(lib, ptrs=(0, 16, 16, 16)) == 1
+    assert _fwd(lib, ptrs=(16, 16, 16, 0)) == 1
+    assert _fwd(lib, ptrs=(18, 16, 16, 16)) == 5
+    assert _fwd(lib, ptrs=(16, 16, 16, 16), lse=ctypes.c_void_p(20)) == 5
+    # empty problems are valid and launch nothing (null pointers allowed)
+    assert _fwd(lib, L=0, ptrs=(0, 0, 0, 0)) == 0
+    assert _fwd(lib, B=0, ptrs=(0, 0, 0, 0)) == 0
+
+
+def test_work_counts(lib):
+    import attention_forward_15_gb300 as af
+    f, b = af.work(4, 16, 1024, 64, af.DENSE)
+    assert f == 4 * 64 * 1024 * 1024 * 64 and b == 4 * 64 * 1024 * 64 * 2
+    f, _ = af.work(2, 32, 4096, 128, af.CAUSAL)
+    assert f == 4 * 128 * (4096 * 4097 // 2) * 64
+    f, b = af.work(8, 16, 8192, 128, af.BLOCK_DIAG, 64)
+    assert f == 4 * 128 * 8192 * 64 * 128 and b == 4 * 128 * 8192 * 128 * 2
+
+
+def test_plan_without_device(lib):
+    import attention_forward_15_gb300 as af
+    p = af.plan(4, 16, 1024, 64, af.DENSE, with_ctas=False)
+    assert p["units"] == 4 * 16 * 4 and p["threads"] == 320 and p["smem_bytes"] <= 232448
+    p = af.plan(1, 16, 16384, 256, af.DENSE, dtype=__import__("torch").bfloat16, with_ctas=False)
+    assert p["units"] == 16 * 128 and p["threads"] == 192

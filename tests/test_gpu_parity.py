@@ -1,0 +1,217 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle on
+the same seeded inputs.
+
+Tolerances (max abs over every compared element): O within 4e-3 for fp16 and
+1.6e-2 for bf16, lse within 1e-3, no NaN or Inf.  Small cases compare every
+element and span several 128-row tiles and a ragged tail; the full-size
+workloads are run in the launch configuration the benchmark times and
+compared on sampled rows (first/last rows of heads and tiles, and random rows)
+that the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_inputs import (BLOCK_DIAG, CAUSAL, DENSE, PAGE_TEST_MATRIX, WORKLOADS, make_qkv,
+                         make_workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = {torch.float16: 4e-3, torch.bfloat16: 1.6e-2}
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module")
+def af():
+    import attention_forward_15_gb300 as m
+    from attention_forward_15_gb300 import _build_ext
+    _build_ext.build()
+    m.load_library()
+    assert torch.cuda.is_available()
+    return m
+
+
+def _run(af, q, k, v, mask, bs, scale, guard=False):
+    dev = torch.device("cuda", 0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    if not guard:
+        o, lse = af.fwd(qd, kd, vd, mask, bs, scale)
+        torch.cuda.synchronize()
+        return o.cpu(), lse.cpu()
+    # outputs carved out of larger buffers whose margins hold a sentinel
+    n = q.numel()
+    pad = 4096
+    ob = torch.full((n + 2 * pad,), float("nan"), dtype=q.dtype, device=dev)
+    lb = torch.full((q.shape[0] * q.shape[1] * q.shape[2] + 2 * pad,), -12345.0,
+                    dtype=torch.float32, device=dev)
+    o = ob[pad:pad + n].view(q.shape)
+    lse = lb[pad:pad + lb.numel() - 2 * pad].view(q.shape[:3])
+    af.fwd(qd, kd, vd, mask, bs, scale, out=o, lse_out=lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(ob[:pad]).all() and torch.isnan(ob[pad + n:]).all(), "O guard overwritten"
+    assert (lb[:pad] == -12345.0).all() and (lb[-pad:] == -12345.0).all(), "lse guard overwritten"
+    return o.cpu(), lse.cpu()
+
+
+def _check(o, lse, O_ref, lse_ref, dtype, what, o_scale=1.0):
+    og = o.double().numpy().reshape(O_ref.shape)
+    lg = lse.double().numpy().reshape(lse_ref.shape)
+    assert np.isfinite(og).all(), f"{what}: non-finite O"
+    assert np.isfinite(lg).all(), f"{what}: non-finite lse"
+    eo = np.abs(og - O_ref).max() if og.size else 0.0
+    el = np.abs(lg - lse_ref).max() if lg.size else 0.0
+    tol = TOL_O[dtype] * o_scale
+    assert eo <= tol, f"{what}: max|dO| = {eo:.3e} > {tol}"
+    assert el <= TOL_LSE, f"{what}: max|dlse| = {el:.3e} > {TOL_LSE}"
+    return eo, el
+
+
+def _full_case(af, B, H, L, D, mask, bs, dtype, scale=None, seed=42, std=1.0, guard=True):
+    q, k, v = make_qkv(B, H, L, D, dtype, seed=seed, std=std)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o, lse = _run(af, q, k, v, mask, bs, scale, guard=guard)
+    O_ref, lse_ref = oracle.attention(q, k, v, mask, bs, scale)
+    # O is linear in V, so its rounding error grows with the spread of V: the
+    # N(0, 1) tolerance is scaled by std for wider inputs.
+    return _check(o, lse, O_ref, lse_ref, dtype, f"B{B} H{H} L{L} D{D} m{mask} bs{bs} {dtype}",
+                  o_scale=max(1.0, std))
+
+
+# --------------------------------------------------------------- small, every element
+
+SMALL = [
+    # (B, H, L, D, mask, bs, dtype)
+    (1, 2, 256, 128, BLOCK_DIAG, 64, torch.float16),     # self-check shape, TLX page
+    (2, 3, 384, 64, DENSE, 0, torch.float16),
+    (1, 2, 300, 64, DENSE, 0, torch.bfloat16),           # ragged tail
+    (1, 3, 640, 128, DENSE, 0, torch.bfloat16),          # odd number of query tiles
+    (2, 2, 200, 128, DENSE, 0, torch.float16),
+    (1, 2, 512, 256, DENSE, 0, torch.bfloat16),
+    (1, 1, 333, 256, DENSE, 0, torch.float16),
+    (2, 2, 512, 128, CAUSAL, 0, torch.bfloat16),
+    (1, 3, 640, 128, CAUSAL, 0, torch.float16),
+    (1, 2, 333, 64, CAUSAL, 0, torch.float16),
+    (1, 2, 384, 256, CAUSAL, 0, torch.bfloat16),
+    (1, 2, 1, 64, CAUSAL, 0, torch.float16),             # a single row
+    (1, 2, 512, 128, BLOCK_DIAG, 1, torch.float16),      # block 1: O = V
+    (1, 2, 512, 64, BLOCK_DIAG, 16, torch.bfloat16),
+    (2, 2, 512, 128, BLOCK_DIAG, 128, torch.float16),
+    (1, 2, 768, 128, BLOCK_DIAG, 256, torch.bfloat16),
+    (1, 2, 768, 64, BLOCK_DIAG, 384, torch.float16),     # blocks of three tiles
+    (1, 2, 512, 256, BLOCK_DIAG, 128, torch.bfloat16),
+    (1, 2, 320, 128, BLOCK_DIAG, 64, torch.float16),     # ragged tail with blocks
+    (1, 2, 512, 128, BLOCK_DIAG, 512, torch.bfloat16),   # block = L: dense
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "B{}H{}L{}D{}m{}bs{}{}".format(
+    *c[:6], "f16" if c[6] == torch.float16 else "bf16"))
+def test_small_all_elements(af, case):
+    _full_case(af, *case)
+
+
+@pytest.mark.parametrize("mask,bs", [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 64)])
+def test_large_scores_exercise_rescaling(af, mask, bs):
+    """N(0, 3^2) inputs: scaled scores have a standard deviation near 9, so the
+    running max keeps jumping by more than the rescale threshold and the O
+    rescale path runs on most rows."""
+    _full_case(af, 1, 2, 512, 128, mask, bs, torch.float16, std=3.0)
+    _full_case(af, 1, 2, 512, 64, mask, bs, torch.bfloat16, std=3.0, scale=0.3)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.125, 1e-3])
+def test_unusual_scales(af, scale):
+    _full_case(af, 1, 2, 384, 128, CAUSAL, 0, torch.float16, scale=scale)
+    _full_case(af, 1, 2, 256, 64, BLOCK_DIAG, 32, torch.float16, scale=scale)
+
+
+@pytest.mark.parametrize("case", PAGE_TEST_MATRIX[:6], ids=str)
+@pytest.mark.parametrize("causal", [False, True])
+def test_page_test_matrix(af, case, causal):
+    """The Fused Attention page's test shapes (seed 20, N(0, 0.5), sm_scale 0.5),
+    plus their causal versions, which the page never ran."""
+    Z, H, N, D, dt = case
+    _full_case(af, Z, H, N, D, CAUSAL if causal else DENSE, 0, dt, scale=0.5, seed=20, std=0.5,
+               guard=False)
+
+
+def test_determinism(af):
+    q, k, v = make_qkv(2, 4, 1024, 128, torch.bfloat16, seed=3)
+    a = _run(af, q, k, v, CAUSAL, 0, 0.1)
+    b = _run(af, q, k, v, CAUSAL, 0, 0.1)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_empty_and_no_lse(af):
+    dev = torch.device("cuda", 0)
+    q = torch.empty((1, 2, 0, 64), dtype=torch.float16, device=dev)
+    o, lse = af.fwd(q, q, q, DENSE)
+    assert o.shape == q.shape and lse.shape == (1, 2, 0)
+    qh, kh, vh = make_qkv(1, 2, 256, 64, torch.float16)
+    o, lse = af.fwd(qh.to(dev), kh.to(dev), vh.to(dev), DENSE, 0, 0.125, return_lse=False)
+    assert lse is None
+    O_ref, _ = oracle.attention(qh, kh, vh, DENSE, 0, 0.125)
+    assert np.abs(o.double().cpu().numpy() - O_ref).max() <= TOL_O[torch.float16]
+
+
+def test_argument_errors(af):
+    dev = torch.device("cuda", 0)
+    q = torch.zeros((1, 1, 256, 96), dtype=torch.float16, device=dev)
+    with pytest.raises(af.AttnError) as e:
+        af.fwd(q, q, q)
+    assert e.value.status == 4                      # head dim 96 unsupported
+    q = torch.zeros((1, 1, 256, 64), dtype=torch.float16, device=dev)
+    with pytest.raises(af.AttnError) as e:
+        af.fwd(q, q, q, BLOCK_DIAG, 48)
+    assert e.value.status == 3                      # 48 does not divide 256
+    with pytest.raises(af.AttnError) as e:
+        af.fwd(q, q, q, BLOCK_DIAG, 0)
+    assert e.value.status == 3
+    with pytest.raises(af.AttnError) as e:
+        af.fwd(q, q, q, DENSE, 0, float("inf"))
+    assert e.value.status == 8
+    big = torch.zeros((1 * 1 * 256 * 64 + 8,), dtype=torch.float16, device=dev)
+    mis = big[1:1 + 256 * 64].view(1, 1, 256, 64)  # 2-byte offset
+    with pytest.raises(af.AttnError) as e:
+        af.fwd(mis, q, q)
+    assert e.value.status == 5
+    assert af.last_device_status(0)[0] == 0
+
+
+# --------------------------------------------------------------- full size, sampled rows
+
+def _sample_rows(B, H, L, n_random, seed):
+    BH = B * H
+    rows = set()
+    for bh in sorted({0, BH // 2, BH - 1}):
+        for i in {0, 1, 127, 128, L // 2, L - 129, L - 128, L - 1}:
+            if 0 <= i < L:
+                rows.add(bh * L + i)
+    g = np.random.default_rng(seed)
+    rows.update(int(r) for r in g.integers(0, BH * L, size=n_random))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+FULL = ["blockdiag_b1h2n256d128_bs64_f16", "dense_b4h16l1024d64_f16", "causal_b2h32l4096d128_bf16",
+        "blockdiag_b8h16n8192d128_bs64_f16", "blockdiag_b8h16n8192d128_bs128_f16",
+        "causal_b1h32l32768d128_bf16", "dense_b1h16l16384d256_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled(af, name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    dev = torch.device("cuda", 0)
+    o, lse = af.fwd(q.to(dev), k.to(dev), v.to(dev), w.mask, w.block_size, w.sm_scale)
+    torch.cuda.synchronize()
+    o = o.cpu()
+    lse = lse.cpu()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    rows = _sample_rows(w.B, w.H, w.L, 192, seed=1)
+    O_ref, lse_ref = oracle.attention(q, k, v, w.mask, w.block_size, w.sm_scale, rows=rows)
+    og = o.reshape(-1, w.D)[torch.from_numpy(rows)]
+    lg = lse.reshape(-1)[torch.from_numpy(rows)]
+    _check(og, lg, O_ref, lse_ref, w.dtype, name)
