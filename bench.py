@@ -291,6 +291,23 @@ def cpu_baseline(w, target_s: float = 10.0):
                       f"{dt:.2f} s wall"}
 
 
+# ----------------------------------------------------------------- ranks
+
+def reduce_max(x: float, dist, dev) -> float:
+    """Max of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs the same per-rank work, timed by
+    the slowest rank."""
+    return flops_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------- main
 
 def roofline_for(w, flops, nbytes, ms, peaks, peaks_kind, traffic):
@@ -344,16 +361,12 @@ def main():
     ms, info = time_workload(af, w, dev, args.steps, args.warmup, soak_s=args.soak_s,
                              sampler=sampler, dist=dist)
     clocks = sampler.stop() if sampler else None
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms, dist, dev)
 
-    e2e_s, h2d, d2h = time_e2e(af, w, dev, max(10, min(args.steps, 200)), 3)
     if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+        dist.barrier()
+    e2e_s, h2d, d2h = time_e2e(af, w, dev, max(10, min(args.steps, 200)), 3)
+    e2e_s = reduce_max(e2e_s, dist, dev)
 
     per_mask = {}
     if not args.no_all:
@@ -375,7 +388,7 @@ def main():
             dist.destroy_process_group()
         return
 
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms)
     cfg = w.describe()
     cfg.update({"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "l2": f"{info['rotating_sets']} rotating input/output sets of "
@@ -391,7 +404,7 @@ def main():
         "dtype": "f16" if w.dtype == torch.float16 else "bf16", "data": "synthetic",
         "config": cfg,
         "roofline": roofline_for(w, flops, nbytes, ms, peaks, peaks_kind, ncu_traffic(w.name)),
-        "e2e": {"value": round(flops * world / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_tflops(flops, world, e2e_s * 1e3), 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": args.steps,
