@@ -34,7 +34,7 @@
 //                         O lane 0 at col 256, O lane 1 at col 256 + D;
 //   single mode (D = 256): one query tile, two S/P buffers at cols 0 and 128
 //                         (consecutive key tiles alternate), O at col 256.
-// P (16-bit, two per column) overwrites the first BN/2 columns of its S.
+// P (16-bit, two per column) overwrites the upper BN/2 columns of its S.
 //
 // Every mbarrier wait is bounded (about one second); on expiry the kernel
 // records a timeout in the status word, tells the other roles to stop through
@@ -86,6 +86,8 @@ struct Cfg {
         return 256u + (PAIR ? static_cast<uint32_t>(w) * D : 0u);
     }
     static constexpr uint32_t TMEM_COLS = 512;
+    // P (16-bit pairs) occupies the upper BN/2 columns of its S buffer
+    static constexpr uint32_t P_OFF = BN / 2;
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * TILE_BYTES;
@@ -222,6 +224,65 @@ enum : unsigned {
     kSitePFull = 6, kSiteSFull = 7, kSiteODone = 8, kSiteDrain = 9
 };
 
+// ------------------------------------------------------- softmax helpers
+
+// Keys of a 64-key half (first key index `base` in the tile) outside
+// [rel_lo, rel_hi) take the value `fill` (excluded from the row extreme).
+__device__ __forceinline__ void mask_half(uint32_t (&v)[64], int base, int rel_lo, int rel_hi,
+                                          float fill) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+        if (base + c < rel_lo || base + c >= rel_hi) v[c] = __float_as_uint(fill);
+}
+
+// max (or min) of 64 raw scores with three-input min/max, four chains.
+__device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool want_max) {
+    float a[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] = __uint_as_float(v[e]);
+    if (want_max) {
+#pragma unroll
+        for (int c = 4; c < 64; c += 8)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                a[e] = fmax3(a[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
+        return fmaxf(fmax3(a[0], a[1], a[2]), a[3]);
+    }
+#pragma unroll
+    for (int c = 4; c < 64; c += 8)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            a[e] = fmin3(a[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
+    return fminf(fmin3(a[0], a[1], a[2]), a[3]);
+}
+
+// p = exp2(s * sc - m) for a 64-key half (keys base..base+63 of the tile):
+// packed fma, MUFU ex2, packed partial sums into acc[8], rounding to 16-bit
+// pairs and one 32-column TMEM store at `dst`.
+template <bool BF16>
+__device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, bool masked, int rel_lo,
+                                         int rel_hi, float sc, float neg_m, float (&acc)[8],
+                                         uint32_t dst) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, neg_m, neg_m);
+        float p0 = ex2_approx(x0);
+        float p1 = ex2_approx(x1);
+        if (masked) {
+            const int c0 = base + 2 * e;
+            if (c0 < rel_lo || c0 >= rel_hi) p0 = 0.f;
+            if (c0 + 1 < rel_lo || c0 + 1 >= rel_hi) p1 = 0.f;
+        }
+        const int k = 2 * (e & 3);
+        fadd2(acc[k], acc[k + 1], acc[k], acc[k + 1], p0, p1);
+        pk[e] = pack2<BF16>(p0, p1);
+    }
+    tmem_st32(dst, pk);
+}
+
+// ---------------------------------------------------------------- kernel
 // ---------------------------------------------------------------- kernel
 
 template <int D, bool BF16, bool PAIR>
@@ -354,7 +415,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const uint32_t vb = ring_smem + vslot * C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C::o_col(ocol_idx), tmem + C::s_col(sbuf) + kk * 8, v_desc(vb, kk),
+                    mma_ts(tmem + C::o_col(ocol_idx), tmem + C::s_col(sbuf) + C::P_OFF + kk * 8, v_desc(vb, kk),
                            IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             };
 
@@ -518,43 +579,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 ++sn[b];
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_off + C::s_col(b);
-                float s[BN];
-                {
-                    uint32_t raw[BN];
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c)
-                        tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(raw[c]);
-                }
+                const uint32_t p_addr = s_addr + C::P_OFF;
                 const bool masked = tile_masked(p, qt, j);
                 const int rel_lo = klo - j * BN, rel_hi = khi - j * BN;
-                if (masked) {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c)
-                        if (c < rel_lo || c >= rel_hi) s[c] = fill;
+                // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
+                // two 64-key halves; the upper half stays in registers.
+                uint32_t hi[64];
+                float ext;
+                {
+                    uint32_t lo[64];
+                    tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                    tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                    tmem_wait_ld();
+                    if (masked) mask_half(lo, 0, rel_lo, rel_hi, fill);
+                    ext = row_extreme64(lo, sc >= 0.f);
                 }
-                // row extreme of the raw scores (max for sm_scale >= 0, else min)
-                float ext[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ext[e] = s[e];
-                if (sc >= 0.f) {
-#pragma unroll
-                    for (int c = 8; c < BN; ++c) ext[c & 7] = fmaxf(ext[c & 7], s[c]);
-#pragma unroll
-                    for (int e = 4; e > 0; e >>= 1)
-#pragma unroll
-                        for (int f = 0; f < e; ++f) ext[f] = fmaxf(ext[f], ext[f + e]);
-                } else {
-#pragma unroll
-                    for (int c = 8; c < BN; ++c) ext[c & 7] = fminf(ext[c & 7], s[c]);
-#pragma unroll
-                    for (int e = 4; e > 0; e >>= 1)
-#pragma unroll
-                        for (int f = 0; f < e; ++f) ext[f] = fminf(ext[f], ext[f + e]);
+                tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
+                tmem_wait_ld();
+                if (masked) mask_half(hi, 64, rel_lo, rel_hi, fill);
+                {
+                    const float e2 = row_extreme64(hi, sc >= 0.f);
+                    ext = sc >= 0.f ? fmaxf(ext, e2) : fminf(ext, e2);
                 }
-                const float m_tile = isinf(ext[0]) ? -INFINITY : ext[0] * sc;
+                const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (t == 0) {
@@ -565,32 +613,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     rescale = true;
                 }
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                float part[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) part[e] = 0.f;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int c0 = 64 * h + 2 * e;
-                        float p0 = ex2_approx(fmaf(s[c0], sc, neg_m));
-                        float p1 = ex2_approx(fmaf(s[c0 + 1], sc, neg_m));
-                        if (masked) {
-                            if (c0 < rel_lo || c0 >= rel_hi) p0 = 0.f;
-                            if (c0 + 1 < rel_lo || c0 + 1 >= rel_hi) p1 = 0.f;
-                        }
-                        part[(2 * e) & 7] += p0;
-                        part[(2 * e + 1) & 7] += p1;
-                        pk[e] = pack2<BF16>(p0, p1);
-                    }
-                    tmem_st32(s_addr + 32 * h, pk);
+                // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
+                // upper half of the S columns: the upper 64 keys first (their S
+                // columns are already in registers), then the lower 64 keys,
+                // reloaded (their P columns overwrite S columns 64..95, consumed).
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                exp_half<BF16>(hi, 64, masked, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                {
+                    uint32_t lo[64];
+                    tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                    tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                    tmem_wait_ld();
+                    exp_half<BF16>(lo, 0, masked, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
                 }
-#pragma unroll
-                for (int e = 4; e > 0; e >>= 1)
-#pragma unroll
-                    for (int f = 0; f < e; ++f) part[f] += part[f + e];
-                l = l * alpha + part[0];
+                fadd2(acc[0], acc[1], acc[0], acc[1], acc[2], acc[3]);
+                fadd2(acc[4], acc[5], acc[4], acc[5], acc[6], acc[7]);
+                fadd2(acc[0], acc[1], acc[0], acc[1], acc[4], acc[5]);
+                l = l * alpha + (acc[0] + acc[1]);
 
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O must hold every earlier P.V before it is rescaled.  In pair
