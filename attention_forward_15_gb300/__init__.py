@@ -182,3 +182,32 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int =
     st["lse_h"].copy_(lse_d, non_blocking=True)
     torch.cuda.current_stream(dev).synchronize()
     return st["o_h"], st["lse_h"]
+
+
+def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                lse: torch.Tensor | None, mask_kind: int = DENSE, block_size: int = 0,
+                sm_scale: float | None = None, status_out: torch.Tensor | None = None):
+    """``attn_fwd_noalloc``: the forward for callers that may not allocate
+    device memory once they are running (the library's own status word lives
+    in a fixed array compiled into it).  The caller passes every buffer,
+    including ``o`` and ``lse``; ``status_out`` is an optional pinned host
+    uint32/int32 tensor of one element that receives this call's device status
+    once the current stream is synchronised.  The first call on a device does
+    a one-time set-up and should come before any stream capture."""
+    lib = load_library()
+    fn = lib.attn_fwd_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = _SIGNATURES["attn_fwd"][1] + [ctypes.c_void_p]
+    B, H, L, D = (int(x) for x in q.shape)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device)
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, H, L, D, int(mask_kind),
+                int(block_size), float(sm_scale), _dtype_code(q.dtype),
+                ctypes.c_void_p(s.cuda_stream),
+                status_out.data_ptr() if status_out is not None else None)
+    if rc:
+        raise AttnError(rc, "attn_fwd_noalloc")
+    return o, lse

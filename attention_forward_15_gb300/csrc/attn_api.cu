@@ -281,3 +281,110 @@ int attn_last_device_status(int device, int *status, unsigned int *detail) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the status word lives in a fixed array compiled
+// into this library instead of memory cudaMalloc'd per device.
+
+namespace {
+
+constexpr int kNoAllocScratchWords = ATTN_NOALLOC_SCRATCH_BYTES / 4;
+static_assert(kNoAllocScratchWords * 4 == ATTN_NOALLOC_SCRATCH_BYTES, "scratch size");
+
+// Word 0: device status of the latest call; the rest is reserved.  Host code
+// must not use this name as a device address: it is a host-side stand-in.
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoAllocScratchWords];
+
+std::mutex g_noalloc_mutex;
+DeviceState g_noalloc_dev[kMaxDevices];   // .status = device address of the array
+
+// Set-up, once per device and with that device current: SM count, tensor-map
+// encoder, the array's device address, and a cleared array.  No allocation.
+int noalloc_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        int rc = load_encoder();
+        if (rc != ATTN_OK) return rc;
+    }
+    std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+    DeviceState &st = g_noalloc_dev[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return ATTN_ERR_CUDA;
+        if (cudaMemset(ptr, 0, ATTN_NOALLOC_SCRATCH_BYTES) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+        st.status = static_cast<unsigned int *>(ptr);
+        st.ready = true;
+    }
+    *out = &st;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int H, int L, int D, int mask_kind, int block_size,
+                                float sm_scale, int dtype, void *stream,
+                                unsigned int *status_out) {
+    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
+    // scratch this kernel needs: one status word, whatever the problem size
+    constexpr size_t kNeeded = sizeof(unsigned int);
+    if (kNeeded > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H * L == 0) {
+        if (status_out) *status_out = 0;
+        return ATTN_OK;
+    }
+    if (!q || !k || !v || !o) return ATTN_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 15u) != 0))
+        return ATTN_ERR_ALIGN;
+
+    DeviceState *st = nullptr;
+    rc = noalloc_state(&st);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(st->status, 0, kNeeded, s) != cudaSuccess) return ATTN_ERR_CUDA;
+
+    const Plan pl = make_plan(B, H, L, D);
+    FwdParams prm;
+    prm.o = o;
+    prm.lse = lse;
+    prm.status = st->status;
+    prm.BH = B * H;
+    prm.L = L;
+    prm.mask = mask_kind;
+    prm.bs = mask_kind == ATTN_MASK_BLOCK_DIAG ? block_size : 0;
+    prm.n_qt = pl.n_qt;
+    prm.n_kv = pl.n_kv;
+    prm.n_units = pl.n_units;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
+
+    const bool bf16 = dtype == ATTN_BF16;
+    switch (D) {
+        case 64:
+            rc = bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
+                      : launch<64, false, true>(*st, q, k, v, prm, dtype, s);
+            break;
+        case 128:
+            rc = bf16 ? launch<128, true, true>(*st, q, k, v, prm, dtype, s)
+                      : launch<128, false, true>(*st, q, k, v, prm, dtype, s);
+            break;
+        default:
+            rc = bf16 ? launch<256, true, false>(*st, q, k, v, prm, dtype, s)
+                      : launch<256, false, false>(*st, q, k, v, prm, dtype, s);
+            break;
+    }
+    if (rc != ATTN_OK) return rc;
+    if (status_out &&
+        cudaMemcpyAsync(status_out, st->status, kNeeded, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}

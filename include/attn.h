@@ -109,6 +109,38 @@ const char *attn_status_string(int status);
  */
 int attn_last_device_status(int device, int *status, unsigned int *detail);
 
+/*
+ * attn_fwd_noalloc -- attn_fwd for callers that may not allocate device
+ * memory: a serving runtime that reserves its whole memory budget at start-up
+ * and forbids later allocations, or a host framework whose own pool must stay
+ * the only owner of device memory.  (The source pages have no counterpart;
+ * this entry point exists for such callers only.)
+ *
+ * Same arguments, layout and results as attn_fwd.  attn_fwd keeps its
+ * device status word in memory the library cudaMallocs on the first call on
+ * each device; this variant instead keeps it in a fixed 256-byte array
+ * compiled into the library (ATTN_NOALLOC_SCRATCH_BYTES per device, held by
+ * every GPU that loads the library until the process exits), and calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   status_out  optional HOST pointer (may be NULL).  If given, the device
+ *               status word of this call (0, or ATTN_ERR_TIMEOUT in its low
+ *               byte) is copied there on `stream`; read it after the stream is
+ *               synchronised (pinned memory keeps the copy asynchronous).
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and clears it; make that first call before any
+ * stream capture.  Every call clears the status word on `stream` and then
+ * launches.  All calls share the one array, so calls that overlap on the GPU
+ * (different streams, no ordering) race on the status word.  The scratch a
+ * call needs does not grow with the problem (one 32-bit word); a call that
+ * would need more than the array holds is refused with ATTN_ERR_UNSUPPORTED.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES 256
+int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int L, int D, int mask_kind, int block_size,
+                     float sm_scale, int dtype, void *stream, unsigned int *status_out);
+
 /* Number of work units and CTAs attn_fwd would launch for these arguments on
  * the current device (for tests and reports); returns an attn_status. */
 int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size,
