@@ -76,6 +76,8 @@ struct Cfg {
     static constexpr int CHUNK_BYTES = 128 * 128;     // one box: 128 rows x 128 bytes
     static constexpr int TILE_BYTES = 128 * D * 2;    // one Q, K or V tile
     static constexpr int RING = D == 64 ? 8 : (D == 128 ? 5 : 2);
+    // pairs of every 8 whose exp2 runs on the FMA pipe (see exp2_emu2)
+    static constexpr int EMU = D == 64 ? 3 : (D == 128 ? 1 : 0);
     static constexpr int NUM_WARPS = 4 * NWG + 2;
     static constexpr int THREADS = 32 * NUM_WARPS;
     static constexpr int WARP_TMA = 4 * NWG;
@@ -224,6 +226,18 @@ enum : unsigned {
     kSitePFull = 6, kSiteSFull = 7, kSiteODone = 8, kSiteDrain = 9
 };
 
+// Two counters selected by a runtime index without a local-memory array.
+struct Count2 {
+    uint32_t v0 = 0, v1 = 0;
+    __device__ __forceinline__ uint32_t get(int i) const { return i ? v1 : v0; }
+    __device__ __forceinline__ void set(int i, uint32_t x) {
+        if (i) v1 = x; else v0 = x;
+    }
+    __device__ __forceinline__ void inc(int i) {
+        if (i) ++v1; else ++v0;
+    }
+};
+
 // ------------------------------------------------------- softmax helpers
 
 // Keys of a 64-key half (first key index `base` in the tile) outside
@@ -232,7 +246,8 @@ __device__ __forceinline__ void mask_half(uint32_t (&v)[64], int base, int rel_l
                                           float fill) {
 #pragma unroll
     for (int c = 0; c < 64; ++c)
-        if (base + c < rel_lo || base + c >= rel_hi) v[c] = __float_as_uint(fill);
+        if (static_cast<unsigned>(base + c - rel_lo) >= static_cast<unsigned>(rel_hi - rel_lo))
+            v[c] = __float_as_uint(fill);
 }
 
 // max (or min) of 64 raw scores with three-input min/max, four chains.
@@ -258,26 +273,55 @@ __device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool wan
 
 // p = exp2(s * sc - m) for a 64-key half (keys base..base+63 of the tile):
 // packed fma, MUFU ex2, packed partial sums into acc[8], rounding to 16-bit
-// pairs and one 32-column TMEM store at `dst`.
-template <bool BF16>
-__device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, bool masked, int rel_lo,
-                                         int rel_hi, float sc, float neg_m, float (&acc)[8],
-                                         uint32_t dst) {
+// pairs and one 32-column TMEM store at `dst`.  The packed fp32x2 builtins
+// let the compiler keep operand pairs in register pairs.
+// exp2 of a pair on the FMA pipe instead of the MUFU: 2^x = 2^j * 2^f with
+// j = round(x) (left in the low mantissa bits of x + 1.5*2^23) and
+// f = x - j in [-1/2, 1/2]; 2^f is a degree-3 polynomial with minimal
+// maximum relative error on [-1/2, 1/2] (Remez exchange, coefficients from
+// fit_exp2_poly.py next to this file); relative error of the fp32 evaluation
+// below 7.5e-5, well under the rounding of P to 16 bits.  x is clamped at
+// -125 so that 2^j stays a normal number (such a p is 0 after rounding anyway).
+__device__ __forceinline__ float2 exp2_emu2(float2 x) {
+    constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+    constexpr float c0 = 0.999928057f, c1 = 0.693260968f, c2 = 0.242611125f, c3 = 0.0551716685f;
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
+    const float2 j = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+    const float2 f = __ffma2_rn(j, make_float2(-1.f, -1.f), x);
+    float2 q = __ffma2_rn(make_float2(c3, c3), f, make_float2(c2, c2));
+    q = __ffma2_rn(q, f, make_float2(c1, c1));
+    q = __ffma2_rn(q, f, make_float2(c0, c0));
+    return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
+}
+
+template <bool BF16, bool MASKED, int EMU>
+__device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, int rel_lo, int rel_hi,
+                                         float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(neg_m, neg_m);
     uint32_t pk[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-        float x0, x1;
-        ffma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, neg_m, neg_m);
-        float p0 = ex2_approx(x0);
-        float p1 = ex2_approx(x1);
-        if (masked) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                    sc2, nm2);
+        // EMU of every 8 pairs go through the FMA-pipe polynomial, the rest
+        // through the MUFU, to balance the two pipes
+        float2 pp;
+        if ((e & 7) < EMU)
+            pp = exp2_emu2(x);
+        else
+            pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if constexpr (MASKED) {
+            const unsigned width = static_cast<unsigned>(rel_hi - rel_lo);
             const int c0 = base + 2 * e;
-            if (c0 < rel_lo || c0 >= rel_hi) p0 = 0.f;
-            if (c0 + 1 < rel_lo || c0 + 1 >= rel_hi) p1 = 0.f;
+            if (static_cast<unsigned>(c0 - rel_lo) >= width) pp.x = 0.f;
+            if (static_cast<unsigned>(c0 + 1 - rel_lo) >= width) pp.y = 0.f;
         }
-        const int k = 2 * (e & 3);
-        fadd2(acc[k], acc[k + 1], acc[k], acc[k + 1], p0, p1);
-        pk[e] = pack2<BF16>(p0, p1);
+        acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
+        pk[e] = pack2<BF16>(pp.x, pp.y);
     }
     tmem_st32(dst, pk);
 }
@@ -347,8 +391,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const int u = unit_of(p, cta, G, r);
                 if (u >= p.n_units) continue;
                 const Unit U = make_unit<PAIR>(p, u);
-                for (int w = 0; w < C::NQ && ok; ++w) {
-                    if (U.qt[w] < 0) continue;
+#pragma unroll
+                for (int w = 0; w < C::NQ; ++w) {
+                    if (!ok || U.qt[w] < 0) continue;
                     ok = wait_bar(bar(C::B_QEMPTY + w), (qn[w] & 1u) ^ 1u, ctl, kSiteQEmpty);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::B_QFULL + w), C::TILE_BYTES);
@@ -360,7 +405,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
                 for (int j = U.ulo; j < U.uhi && ok; ++j) {
                     if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
-                    for (int kind = 0; kind < 2 && ok; ++kind) {
+#pragma unroll
+                    for (int kind = 0; kind < 2; ++kind) {
+                        if (!ok) continue;
                         const uint32_t slot = rc % C::RING;
                         ok = wait_bar(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u, ctl,
                                       kSiteKvEmpty);
@@ -394,29 +441,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             constexpr uint32_t IDESC_PV = idesc_f16_f32acc(BF16, BM, D, true);
             const uint32_t q_smem = s_base + C::OFF_Q;
             const uint32_t ring_smem = s_base + C::OFF_RING;
+            // Descriptors advance by adding to their 16-byte-unit address field.
             // S = Q K^T: k-step kk covers head-dim columns [16kk, 16kk+16): box kk/4,
             // 32-byte offset (kk%4) inside the 128-byte swizzled row.
-            auto qk_desc = [&](uint32_t base, int kk) -> uint64_t {
-                return sdesc_sw128(base + (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32, 16, 1024);
+            auto issue_s = [&](int w, int sbuf, uint32_t kslot) {
+                const uint64_t qd = sdesc_sw128(q_smem + w * C::TILE_BYTES, 16, 1024);
+                const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::TILE_BYTES, 16, 1024);
+                const uint32_t d_tmem = tmem + C::s_col(sbuf);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
+                    mma_ss(d_tmem, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                }
             };
             // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
-            // consecutive 64-column boxes of V are C::CHUNK_BYTES apart.
-            auto v_desc = [&](uint32_t base, int kk) -> uint64_t {
-                return sdesc_sw128(base + kk * 16 * 128, C::CHUNK_BYTES, 1024);
-            };
-            auto issue_s = [&](int w, int sbuf, uint32_t kslot) {
-                const uint32_t qb = q_smem + w * C::TILE_BYTES;
-                const uint32_t kb = ring_smem + kslot * C::TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::s_col(sbuf), qk_desc(qb, kk), qk_desc(kb, kk), IDESC_S, kk > 0);
-            };
+            // consecutive 64-column boxes of V are C::CHUNK_BYTES apart (LBO).
             auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
-                const uint32_t vb = ring_smem + vslot * C::TILE_BYTES;
+                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+                const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
+                const uint32_t a_tmem = tmem + C::s_col(sbuf) + C::P_OFF;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C::o_col(ocol_idx), tmem + C::s_col(sbuf) + C::P_OFF + kk * 8, v_desc(vb, kk),
-                           IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
+                           (accumulate || kk > 0) ? 1u : 0u);
             };
 
             uint32_t rc = 0;
@@ -427,8 +474,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const int u = unit_of(p, cta, G, r);
                 if (u >= p.n_units) continue;
                 const Unit U = make_unit<PAIR>(p, u);
-                for (int w = 0; w < C::NQ && ok; ++w) {
-                    if (U.qt[w] < 0) continue;
+#pragma unroll
+                for (int w = 0; w < C::NQ; ++w) {
+                    if (!ok || U.qt[w] < 0) continue;
                     ok = wait_bar(bar(C::B_QFULL + w), qn[w] & 1u, ctl, kSiteQFull);
                     ++qn[w];
                 }
@@ -464,8 +512,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                       kSiteKvFullK);
                         if (!ok) break;
                         tc_fence_after();
-                        for (int w = 0; w < 2 && ok; ++w) {
-                            if (!(w == 0 ? use0 : use1)) continue;
+#pragma unroll
+                        for (int w = 0; w < 2; ++w) {
+                            if (!ok || !(w == 0 ? use0 : use1)) continue;
                             if (pend_j[w] >= 0) ok = flush_pv(w);
                             if (!ok) break;
                             issue_s(w, w, kslot);
@@ -476,8 +525,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         }
                         if (ok) mma_commit(bar(C::B_KVEMPTY + kslot));
                     }
-                    for (int w = 0; w < 2 && ok; ++w)
-                        if (pend_j[w] >= 0) ok = flush_pv(w);
+#pragma unroll
+                    for (int w = 0; w < 2; ++w)
+                        if (ok && pend_j[w] >= 0) ok = flush_pv(w);
                 } else {
                     // One query tile, S buffers alternate: S(0), S(1), PV(0), S(2), PV(1), ...
                     const int n = U.hi[0] - U.lo[0];
@@ -530,9 +580,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float sc = p.scale_log2;
         const float fill = sc >= 0.f ? -INFINITY : INFINITY;
-        uint32_t sn[2] = {0, 0};      // S-ready waits per buffer
-        uint32_t made[2] = {0, 0};    // P tiles handed to the MMA warp per buffer
-        uint32_t seen[2] = {0, 0};    // P.V completions confirmed per buffer
+        Count2 sn, made, seen;        // per S buffer: S-ready waits, P tiles handed
+                                      // to the MMA warp, P.V completions confirmed
         bool ok = true;
 
         // All 32 lanes poll; the outcome is made warp-uniform so that the
@@ -542,9 +591,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             return __all_sync(0xffffffffu, r);
         };
         auto wait_pv = [&](int b) -> bool {
-            if (seen[b] < made[b]) {
-                if (!wait_warp(bar(C::B_ODONE + b), (made[b] - 1) & 1u, kSiteODone)) return false;
-                seen[b] = made[b];
+            if (seen.get(b) < made.get(b)) {
+                if (!wait_warp(bar(C::B_ODONE + b), (made.get(b) - 1) & 1u, kSiteODone)) return false;
+                seen.set(b, made.get(b));
             }
             return true;
         };
@@ -553,7 +602,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const int u = unit_of(p, cta, G, r);
             if (u >= p.n_units) continue;
             const Unit U = make_unit<PAIR>(p, u);
-            const int qt = U.qt[wg];
+            const int qt = wg ? U.qt[1] : U.qt[0];
+            const int j_lo = wg ? U.lo[1] : U.lo[0];
+            const int j_hi = wg ? U.hi[1] : U.hi[0];
             if (qt < 0) continue;
             const int i = qt * BM + row;                // query row in the head
             const bool row_valid = i < p.L;
@@ -572,11 +623,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             float m_ref = -INFINITY;                    // running max (log2 units, may lag)
             float l = 0.f;                              // running denominator
             int t = 0;
-            for (int j = U.lo[wg]; j < U.hi[wg] && ok; ++j, ++t) {
+            for (int j = j_lo; j < j_hi && ok; ++j, ++t) {
                 const int b = PAIR ? wg : (t & 1);
-                ok = wait_warp(bar(C::B_SFULL + b), sn[b] & 1u, kSiteSFull);
+                ok = wait_warp(bar(C::B_SFULL + b), sn.get(b) & 1u, kSiteSFull);
                 if (!ok) break;
-                ++sn[b];
+                sn.inc(b);
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_off + C::s_col(b);
                 const uint32_t p_addr = s_addr + C::P_OFF;
@@ -617,19 +668,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // upper half of the S columns: the upper 64 keys first (their S
                 // columns are already in registers), then the lower 64 keys,
                 // reloaded (their P columns overwrite S columns 64..95, consumed).
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                exp_half<BF16>(hi, 64, masked, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                // (the element-wise mask exists only in the masked instantiation,
+                // chosen once per tile)
+                if (masked)
+                    exp_half<BF16, true, C::EMU>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                else
+                    exp_half<BF16, false, C::EMU>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
                 {
                     uint32_t lo[64];
                     tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
                     tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
                     tmem_wait_ld();
-                    exp_half<BF16>(lo, 0, masked, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                    if (masked)
+                        exp_half<BF16, true, C::EMU>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                    else
+                        exp_half<BF16, false, C::EMU>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
                 }
-                fadd2(acc[0], acc[1], acc[0], acc[1], acc[2], acc[3]);
-                fadd2(acc[4], acc[5], acc[4], acc[5], acc[6], acc[7]);
-                fadd2(acc[0], acc[1], acc[0], acc[1], acc[4], acc[5]);
-                l = l * alpha + (acc[0] + acc[1]);
+                acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                l = l * alpha + (acc[0].x + acc[0].y);
 
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O must hold every earlier P.V before it is rescaled.  In pair
@@ -654,7 +712,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
-                ++made[b];
+                made.inc(b);
             }
             if (!ok) break;
             // ------------------------------------------------ epilogue: O / l, lse
