@@ -275,7 +275,7 @@ int attn_last_device_status(int device, int *status, unsigned int *detail) {
     }
     cudaSetDevice(prev);
     if (rc != ATTN_OK) return rc;
-    *status = (word & 0xffu) == attn::kStatusTimeout ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    *status = static_cast<int>(word & 0xffu);   // 0, ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA
     if (detail) *detail = word;
     return ATTN_OK;
 }

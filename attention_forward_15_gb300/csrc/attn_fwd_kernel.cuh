@@ -55,6 +55,7 @@ constexpr int BN = 128;                       // keys per tile
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only if the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr unsigned kStatusTimeout = 7u;       // == ATTN_ERR_TIMEOUT
+constexpr unsigned kStatusTmem = 6u;          // == ATTN_ERR_CUDA: TMEM base not at column 0
 
 enum : int { kMaskDense = 0, kMaskCausal = 1, kMaskBlock = 2 };
 
@@ -347,7 +348,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const int lane = threadIdx.x & 31;
     const int G = gridDim.x;
     const int cta = blockIdx.x;
-    const int rounds = (p.n_units + G - 1) / G;
+    const int rounds_all = (p.n_units + G - 1) / G;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL + 0), 1);
@@ -379,11 +380,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = misc[0];
+    // Allocating all 512 columns can only start at lane 0, column 0, so the TMEM
+    // base is the constant 0 (which keeps every TMEM address a compile-time
+    // offset).  Anything else is reported and no work is done.
+    constexpr uint32_t tmem = 0;
+    const bool tmem_ok = misc[0] == 0u;
+    if (!tmem_ok && threadIdx.x == 0) atomicCAS(p.status, 0u, kStatusTmem);
+
+    // Waits in every role are polled by all 32 lanes and their outcome made
+    // warp-uniform, so warp-collective instructions after them never diverge.
+    auto wait_warp = [&](uint32_t bar_addr, uint32_t parity, unsigned site) -> bool {
+        const bool r = wait_bar(bar_addr, parity, ctl, site);
+        return __all_sync(0xffffffffu, r);
+    };
+
+    const int rounds = tmem_ok ? rounds_all : 0;
 
     if (warp == C::WARP_TMA) {
         // ================================================================ TMA producer
-        if (lane == 0) {
+        // (the whole warp runs this loop; one elected lane issues each copy)
+        {
             uint32_t rc = 0;             // K/V ring position
             uint32_t qn[2] = {0, 0};     // Q loads issued per slot
             bool ok = true;
@@ -394,7 +410,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
                 for (int w = 0; w < C::NQ; ++w) {
                     if (!ok || U.qt[w] < 0) continue;
-                    ok = wait_bar(bar(C::B_QEMPTY + w), (qn[w] & 1u) ^ 1u, ctl, kSiteQEmpty);
+                    ok = wait_warp(bar(C::B_QEMPTY + w), (qn[w] & 1u) ^ 1u, kSiteQEmpty);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::B_QFULL + w), C::TILE_BYTES);
                     const uint32_t dst = s_base + C::OFF_Q + w * C::TILE_BYTES;
@@ -409,8 +425,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     for (int kind = 0; kind < 2; ++kind) {
                         if (!ok) continue;
                         const uint32_t slot = rc % C::RING;
-                        ok = wait_bar(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u, ctl,
-                                      kSiteKvEmpty);
+                        ok = wait_warp(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u,
+                                       kSiteKvEmpty);
                         if (!ok) break;
                         mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::TILE_BYTES);
                         const uint32_t dst = s_base + C::OFF_RING + slot * C::TILE_BYTES;
@@ -436,7 +452,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
+        // (the whole warp runs this loop; one elected lane -- always the same
+        // one, so its commits cover its MMAs -- issues each tcgen05 instruction)
+        {
             constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_f16_f32acc(BF16, BM, D, true);
             const uint32_t q_smem = s_base + C::OFF_Q;
@@ -477,7 +495,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
                 for (int w = 0; w < C::NQ; ++w) {
                     if (!ok || U.qt[w] < 0) continue;
-                    ok = wait_bar(bar(C::B_QFULL + w), qn[w] & 1u, ctl, kSiteQFull);
+                    ok = wait_warp(bar(C::B_QFULL + w), qn[w] & 1u, kSiteQFull);
                     ++qn[w];
                 }
                 if (!ok) break;
@@ -487,11 +505,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     uint32_t pend_v[2] = {0, 0};
                     int npv[2] = {0, 0};
                     auto flush_pv = [&](int w) -> bool {
-                        if (!wait_bar(bar(C::B_PFULL + w), pn[w] & 1u, ctl, kSitePFull)) return false;
+                        if (!wait_warp(bar(C::B_PFULL + w), pn[w] & 1u, kSitePFull)) return false;
                         ++pn[w];
                         const uint32_t vslot = pend_v[w] % C::RING;
-                        if (!wait_bar(bar(C::B_KVFULL + vslot), (pend_v[w] / C::RING) & 1u, ctl,
-                                      kSiteKvFullV))
+                        if (!wait_warp(bar(C::B_KVFULL + vslot), (pend_v[w] / C::RING) & 1u,
+                                       kSiteKvFullV))
                             return false;
                         tc_fence_after();
                         issue_pv(w, w, vslot, npv[w] > 0);
@@ -508,8 +526,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         const uint32_t kpos = rc, vpos = rc + 1;
                         rc += 2;
                         const uint32_t kslot = kpos % C::RING;
-                        ok = wait_bar(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u, ctl,
-                                      kSiteKvFullK);
+                        ok = wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
+                                       kSiteKvFullK);
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
@@ -536,8 +554,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     auto do_s = [&](int t) -> bool {
                         const uint32_t kpos = base + 2u * t;
                         const uint32_t kslot = kpos % C::RING;
-                        if (!wait_bar(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u, ctl,
-                                      kSiteKvFullK))
+                        if (!wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
+                                       kSiteKvFullK))
                             return false;
                         tc_fence_after();
                         issue_s(0, t & 1, kslot);
@@ -551,13 +569,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (t + 1 < n) ok = do_s(t + 1);
                         if (!ok) break;
                         const int b = t & 1;
-                        ok = wait_bar(bar(C::B_PFULL + b), pn[b] & 1u, ctl, kSitePFull);
+                        ok = wait_warp(bar(C::B_PFULL + b), pn[b] & 1u, kSitePFull);
                         if (!ok) break;
                         ++pn[b];
                         const uint32_t vpos = base + 2u * t + 1u;
                         const uint32_t vslot = vpos % C::RING;
-                        ok = wait_bar(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u, ctl,
-                                      kSiteKvFullV);
+                        ok = wait_warp(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u,
+                                       kSiteKvFullV);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(b, 0, vslot, t > 0);
@@ -584,12 +602,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                       // to the MMA warp, P.V completions confirmed
         bool ok = true;
 
-        // All 32 lanes poll; the outcome is made warp-uniform so that the
-        // warp-collective tcgen05 instructions after a wait never diverge.
-        auto wait_warp = [&](uint32_t bar_addr, uint32_t parity, unsigned site) -> bool {
-            const bool r = wait_bar(bar_addr, parity, ctl, site);
-            return __all_sync(0xffffffffu, r);
-        };
         auto wait_pv = [&](int b) -> bool {
             if (seen.get(b) < made.get(b)) {
                 if (!wait_warp(bar(C::B_ODONE + b), (made.get(b) - 1) & 1u, kSiteODone)) return false;

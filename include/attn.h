@@ -103,8 +103,10 @@ const char *attn_status_string(int status);
 /*
  * attn_last_device_status -- read and clear the device status word of CUDA
  * device `device` (the word in-kernel timeouts write).  Synchronises that
- * device first.  *status receives ATTN_OK or ATTN_ERR_TIMEOUT; *detail (may
- * be NULL) receives the raw word (role and wait site of the first timeout).
+ * device first.  *status receives ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA
+ * when a kernel found its tensor memory somewhere it cannot be (and did no
+ * work); *detail (may be NULL) receives the raw word (the wait site of the
+ * first timeout in bits 8-15).
  * Returns an attn_status for the query itself.
  */
 int attn_last_device_status(int device, int *status, unsigned int *detail);
@@ -124,9 +126,10 @@ int attn_last_device_status(int device, int *status, unsigned int *detail);
  * cudaMalloc, cudaFree or other allocating routine.
  *
  *   status_out  optional HOST pointer (may be NULL).  If given, the device
- *               status word of this call (0, or ATTN_ERR_TIMEOUT in its low
- *               byte) is copied there on `stream`; read it after the stream is
- *               synchronised (pinned memory keeps the copy asynchronous).
+ *               status word of this call (0, or an attn_status in its low
+ *               byte, as attn_last_device_status reports) is copied there on
+ *               `stream`; read it after the stream is synchronised (pinned
+ *               memory keeps the copy asynchronous).
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and clears it; make that first call before any
