@@ -83,14 +83,20 @@ struct Cfg {
     static constexpr int THREADS = 32 * NUM_WARPS;
     static constexpr int WARP_TMA = 4 * NWG;
     static constexpr int WARP_MMA = 4 * NWG + 1;
-    // TMEM column of S/P buffer b and of the O accumulator of lane w
+    // SEP: P has columns of its own (D = 64 leaves room), so the next S of a
+    // lane can be computed while the softmax still works on the current one.
+    static constexpr bool SEP = PAIR && D == 64;
+    // TMEM columns of S buffer b, of P buffer b and of the O accumulator of lane w.
+    // Without SEP, P (16-bit pairs) occupies the upper BN/2 columns of its S.
     __device__ static constexpr uint32_t s_col(int b) { return static_cast<uint32_t>(b) * 128u; }
+    __device__ static constexpr uint32_t p_col(int b) {
+        return SEP ? 256u + static_cast<uint32_t>(b) * 64u : s_col(b) + BN / 2;
+    }
     __device__ static constexpr uint32_t o_col(int w) {
-        return 256u + (PAIR ? static_cast<uint32_t>(w) * D : 0u);
+        return SEP ? 384u + static_cast<uint32_t>(w) * 64u
+                   : 256u + (PAIR ? static_cast<uint32_t>(w) * D : 0u);
     }
     static constexpr uint32_t TMEM_COLS = 512;
-    // P (16-bit pairs) occupies the upper BN/2 columns of its S buffer
-    static constexpr uint32_t P_OFF = BN / 2;
     // shared memory (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * TILE_BYTES;
@@ -101,7 +107,8 @@ struct Cfg {
     static constexpr int B_SFULL = B_KVEMPTY + RING;
     static constexpr int B_PFULL = B_SFULL + 2;
     static constexpr int B_ODONE = B_PFULL + 2;
-    static constexpr int B_DRAIN = B_ODONE + 2;
+    static constexpr int B_SFREE = B_ODONE + 2;     // SEP: S buffer read by the softmax
+    static constexpr int B_DRAIN = B_SFREE + 2;
     static constexpr int NBAR = B_DRAIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // [0]: TMEM base, [1]: abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -224,7 +231,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
 // wait sites (recorded in the status word on a timeout)
 enum : unsigned {
     kSiteQEmpty = 1, kSiteKvEmpty = 2, kSiteQFull = 3, kSiteKvFullK = 4, kSiteKvFullV = 5,
-    kSitePFull = 6, kSiteSFull = 7, kSiteODone = 8, kSiteDrain = 9
+    kSitePFull = 6, kSiteSFull = 7, kSiteODone = 8, kSiteDrain = 9, kSiteSFree = 10
 };
 
 // Two counters selected by a runtime index without a local-memory array.
@@ -363,6 +370,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(C::B_SFULL + b), 1);
             mbar_init(bar(C::B_PFULL + b), 4);   // one arrival per softmax warp
             mbar_init(bar(C::B_ODONE + b), 1);
+            mbar_init(bar(C::B_SFREE + b), 4);   // one arrival per softmax warp
         }
         mbar_init(bar(C::B_DRAIN), 1);
         misc[1] = 0;
@@ -477,7 +485,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
                 const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
                 const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
-                const uint32_t a_tmem = tmem + C::s_col(sbuf) + C::P_OFF;
+                const uint32_t a_tmem = tmem + C::p_col(sbuf);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
@@ -487,6 +495,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             uint32_t rc = 0;
             uint32_t qn[2] = {0, 0};
             uint32_t pn[2] = {0, 0};     // P-ready waits per S buffer
+            uint32_t sfn[2] = {0, 0};    // SEP: S issues per lane (S-free waits)
             bool ok = true;
             for (int r = 0; r < rounds && ok; ++r) {
                 const int u = unit_of(p, cta, G, r);
@@ -500,7 +509,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
                 if (!ok) break;
                 tc_fence_after();
-                if constexpr (PAIR) {
+                if constexpr (C::SEP) {
+                    // Per key tile: S of both lanes as soon as their softmax has read
+                    // the previous S, then the P.V of the previous tiles as their P
+                    // arrives.  A lane's P.V(t) is issued after its S(t+1).
+                    int pend_j[2] = {-1, -1};
+                    uint32_t pend_v[2] = {0, 0};
+                    int npv[2] = {0, 0};
+                    auto flush_pv = [&](int w) -> bool {
+                        if (!wait_warp(bar(C::B_PFULL + w), pn[w] & 1u, kSitePFull)) return false;
+                        ++pn[w];
+                        const uint32_t vslot = pend_v[w] % C::RING;
+                        if (!wait_warp(bar(C::B_KVFULL + vslot), (pend_v[w] / C::RING) & 1u,
+                                       kSiteKvFullV))
+                            return false;
+                        tc_fence_after();
+                        issue_pv(w, w, vslot, npv[w] > 0);
+                        ++npv[w];
+                        mma_commit(bar(C::B_ODONE + w));
+                        const bool other_needs = pend_j[1 - w] == pend_j[w];
+                        pend_j[w] = -1;
+                        if (!other_needs) mma_commit(bar(C::B_KVEMPTY + vslot));
+                        return true;
+                    };
+                    for (int j = U.ulo; j < U.uhi && ok; ++j) {
+                        const bool use0 = lane_uses(U, 0, j), use1 = lane_uses(U, 1, j);
+                        if (!use0 && !use1) continue;
+                        const uint32_t kpos = rc, vpos = rc + 1;
+                        rc += 2;
+                        const uint32_t kslot = kpos % C::RING;
+                        ok = wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
+                                       kSiteKvFullK);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int w = 0; w < 2; ++w) {
+                            if (!ok || !(w == 0 ? use0 : use1)) continue;
+                            ok = wait_warp(bar(C::B_SFREE + w), (sfn[w] & 1u) ^ 1u, kSiteSFree);
+                            if (!ok) break;
+                            ++sfn[w];
+                            tc_fence_after();
+                            issue_s(w, w, kslot);
+                            mma_commit(bar(C::B_SFULL + w));
+                            if (j == U.hi[w] - 1) mma_commit(bar(C::B_QEMPTY + w));
+                        }
+                        if (!ok) break;
+                        mma_commit(bar(C::B_KVEMPTY + kslot));
+#pragma unroll
+                        for (int w = 0; w < 2; ++w)
+                            if (ok && pend_j[w] >= 0) ok = flush_pv(w);
+                        if (use0) { pend_j[0] = j; pend_v[0] = vpos; }
+                        if (use1) { pend_j[1] = j; pend_v[1] = vpos; }
+                    }
+#pragma unroll
+                    for (int w = 0; w < 2; ++w)
+                        if (ok && pend_j[w] >= 0) ok = flush_pv(w);
+                } else if constexpr (PAIR) {
                     int pend_j[2] = {-1, -1};
                     uint32_t pend_v[2] = {0, 0};
                     int npv[2] = {0, 0};
@@ -642,7 +706,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 sn.inc(b);
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_off + C::s_col(b);
-                const uint32_t p_addr = s_addr + C::P_OFF;
+                const uint32_t p_addr = tmem + lane_off + C::p_col(b);
                 const bool masked = tile_masked(p, qt, j);
                 const int rel_lo = klo - j * BN, rel_hi = khi - j * BN;
                 // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
@@ -676,6 +740,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     rescale = true;
                 }
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                if constexpr (C::SEP) {
+                    // P and O of this lane are still read/written by the previous
+                    // tile's P.V until it completes.
+                    if (t > 0) {
+                        ok = wait_pv(wg);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                }
                 // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
                 // upper half of the S columns: the upper 64 keys first (their S
                 // columns are already in registers), then the lower 64 keys,
@@ -693,6 +766,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
                     tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
                     tmem_wait_ld();
+                    if constexpr (C::SEP) {
+                        // last read of this S: the MMA warp may overwrite it now
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
+                    }
                     if (masked)
                         exp_half<BF16, true, C::EMU>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
                     else
@@ -705,7 +784,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     // O must hold every earlier P.V before it is rescaled.  In pair
                     // mode the S-ready commit already covered it; in single mode
                     // the previous tile's P.V used the other buffer.
-                    if (!PAIR) ok = wait_pv(b ^ 1);
+                    if constexpr (!PAIR) ok = wait_pv(b ^ 1);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t o_addr = tmem + lane_off + C::o_col(PAIR ? wg : 0);
