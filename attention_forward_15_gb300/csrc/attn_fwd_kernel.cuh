@@ -76,9 +76,14 @@ struct Cfg {
     static constexpr int CHUNKS = D / 64;             // 128-byte-wide TMA boxes per row
     static constexpr int CHUNK_BYTES = 128 * 128;     // one box: 128 rows x 128 bytes
     static constexpr int TILE_BYTES = 128 * D * 2;    // one Q, K or V tile
-    static constexpr int RING = D == 64 ? 8 : (D == 128 ? 5 : 2);
+    // K/V ring entries: a whole tile, or (D = 256) half a tile along the head
+    // dim, so that a deeper ring fits next to the 64 KB Q tile
+    static constexpr int EPT = D == 256 ? 2 : 1;                 // entries per tile
+    static constexpr int ENTRY_BYTES = TILE_BYTES / EPT;
+    static constexpr int ENTRY_CHUNKS = CHUNKS / EPT;
+    static constexpr int RING = D == 64 ? 8 : 5;
     // pairs of every 8 whose exp2 runs on the FMA pipe (see exp2_emu2)
-    static constexpr int EMU = D == 64 ? 3 : (D == 128 ? 1 : 0);
+    static constexpr int EMU = 0;
     static constexpr int NUM_WARPS = 4 * NWG + 2;
     static constexpr int THREADS = 32 * NUM_WARPS;
     static constexpr int WARP_TMA = 4 * NWG;
@@ -98,11 +103,14 @@ struct Cfg {
     }
     static constexpr uint32_t TMEM_COLS = 512;
     // shared memory (offsets from a 1024-byte aligned base)
+    // Q slots: NQB buffers per lane, so the next unit's Q (and the K/V behind it)
+    // can load while the current unit runs; slot (lane w, buffer qb) = qb*NQ + w
+    static constexpr int NQB = D == 64 ? 2 : 1;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_RING = NQ * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_RING + RING * TILE_BYTES;
+    static constexpr int OFF_RING = NQB * NQ * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + RING * ENTRY_BYTES;
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4;
+    static constexpr int B_QFULL = 0, B_QEMPTY = 4, B_KVFULL = 8;
     static constexpr int B_KVEMPTY = B_KVFULL + RING;
     static constexpr int B_SFULL = B_KVEMPTY + RING;
     static constexpr int B_PFULL = B_SFULL + 2;
@@ -116,6 +124,7 @@ struct Cfg {
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
     static_assert(PAIR ? (2 * 128 + 2 * D <= 512) : (D == 256), "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(PAIR ? EPT == 1 : true, "pair modes keep whole-tile ring entries");
 };
 
 // ------------------------------------------------------------ work units
@@ -358,10 +367,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const int rounds_all = (p.n_units + G - 1) / G;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_QFULL + 0), 1);
-        mbar_init(bar(C::B_QFULL + 1), 1);
-        mbar_init(bar(C::B_QEMPTY + 0), 1);
-        mbar_init(bar(C::B_QEMPTY + 1), 1);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(bar(C::B_QFULL + q), 1);
+            mbar_init(bar(C::B_QEMPTY + q), 1);
+        }
         for (int s = 0; s < C::RING; ++s) {
             mbar_init(bar(C::B_KVFULL + s), 1);
             mbar_init(bar(C::B_KVEMPTY + s), 1);
@@ -409,39 +418,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         // (the whole warp runs this loop; one elected lane issues each copy)
         {
             uint32_t rc = 0;             // K/V ring position
-            uint32_t qn[2] = {0, 0};     // Q loads issued per slot
+            uint32_t qpar = 0;           // bit q: parity of the loads into Q slot q
+            uint32_t qused = 0;          // bit q: Q slot q has been loaded
+            uint32_t nunit = 0;          // units of this CTA so far
             bool ok = true;
             for (int r = 0; r < rounds && ok; ++r) {
                 const int u = unit_of(p, cta, G, r);
                 if (u >= p.n_units) continue;
                 const Unit U = make_unit<PAIR>(p, u);
+                const int qb = C::NQB == 2 ? static_cast<int>(nunit & 1u) : 0;
+                ++nunit;
 #pragma unroll
                 for (int w = 0; w < C::NQ; ++w) {
                     if (!ok || U.qt[w] < 0) continue;
-                    ok = wait_warp(bar(C::B_QEMPTY + w), (qn[w] & 1u) ^ 1u, kSiteQEmpty);
+                    const int q = qb * C::NQ + w;
+                    ok = wait_warp(bar(C::B_QEMPTY + q), ((qpar >> q) & 1u) ^ 1u, kSiteQEmpty);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(C::B_QFULL + w), C::TILE_BYTES);
-                    const uint32_t dst = s_base + C::OFF_Q + w * C::TILE_BYTES;
+                    mbar_arrive_expect_tx(bar(C::B_QFULL + q), C::TILE_BYTES);
+                    const uint32_t dst = s_base + C::OFF_Q + q * C::TILE_BYTES;
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_3d(dst + c * C::CHUNK_BYTES, &tmap_q, c * 64, U.qt[w] * BM, U.bh,
-                                    bar(C::B_QFULL + w));
-                    ++qn[w];
+                                    bar(C::B_QFULL + q));
+                    qpar ^= 1u << q;
+                    qused |= 1u << q;
                 }
                 for (int j = U.ulo; j < U.uhi && ok; ++j) {
                     if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
 #pragma unroll
-                    for (int kind = 0; kind < 2; ++kind) {
+                    for (int ke = 0; ke < 2 * C::EPT; ++ke) {   // K entries, then V entries
                         if (!ok) continue;
+                        const int kind = ke / C::EPT, e = ke % C::EPT;
                         const uint32_t slot = rc % C::RING;
                         ok = wait_warp(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u,
                                        kSiteKvEmpty);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::TILE_BYTES);
-                        const uint32_t dst = s_base + C::OFF_RING + slot * C::TILE_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::ENTRY_BYTES);
+                        const uint32_t dst = s_base + C::OFF_RING + slot * C::ENTRY_BYTES;
                         const CUtensorMap *m = kind == 0 ? &tmap_k : &tmap_v;
-                        for (int c = 0; c < C::CHUNKS; ++c)
-                            tma_load_3d(dst + c * C::CHUNK_BYTES, m, c * 64, j * BN, U.bh,
-                                        bar(C::B_KVFULL + slot));
+                        for (int c = 0; c < C::ENTRY_CHUNKS; ++c)
+                            tma_load_3d(dst + c * C::CHUNK_BYTES, m, (e * C::ENTRY_CHUNKS + c) * 64,
+                                        j * BN, U.bh, bar(C::B_KVFULL + slot));
                         ++rc;
                     }
                 }
@@ -452,9 +468,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const uint32_t first = rc > static_cast<uint32_t>(C::RING) ? rc - C::RING : 0u;
                 for (uint32_t i = first; i < rc; ++i)
                     wait_slow(bar(C::B_KVFULL + i % C::RING), (i / C::RING) & 1u, ctl, kSiteDrain, false);
-                for (int w = 0; w < C::NQ; ++w)
-                    if (qn[w] > 0)
-                        wait_slow(bar(C::B_QFULL + w), (qn[w] - 1) & 1u, ctl, kSiteDrain, false);
+                for (int q = 0; q < 4; ++q)
+                    if ((qused >> q) & 1u)   // the latest load of slot q has parity !bit
+                        wait_slow(bar(C::B_QFULL + q), ((qpar >> q) & 1u) ^ 1u, ctl, kSiteDrain, false);
             }
         }
         __syncwarp();
@@ -470,9 +486,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             // Descriptors advance by adding to their 16-byte-unit address field.
             // S = Q K^T: k-step kk covers head-dim columns [16kk, 16kk+16): box kk/4,
             // 32-byte offset (kk%4) inside the 128-byte swizzled row.
-            auto issue_s = [&](int w, int sbuf, uint32_t kslot) {
-                const uint64_t qd = sdesc_sw128(q_smem + w * C::TILE_BYTES, 16, 1024);
-                const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::TILE_BYTES, 16, 1024);
+            auto issue_s = [&](int qslot, int sbuf, uint32_t kslot) {
+                const uint64_t qd = sdesc_sw128(q_smem + qslot * C::TILE_BYTES, 16, 1024);
+                const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::ENTRY_BYTES, 16, 1024);
                 const uint32_t d_tmem = tmem + C::s_col(sbuf);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -483,7 +499,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
             // consecutive 64-column boxes of V are C::CHUNK_BYTES apart (LBO).
             auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
-                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, C::CHUNK_BYTES, 1024);
                 const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
                 const uint32_t a_tmem = tmem + C::p_col(sbuf);
 #pragma unroll
@@ -493,7 +509,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             };
 
             uint32_t rc = 0;
-            uint32_t qn[2] = {0, 0};
+            uint32_t qpar = 0;           // bit q: parity of the Q-full waits of slot q
+            uint32_t nunit = 0;
             uint32_t pn[2] = {0, 0};     // P-ready waits per S buffer
             uint32_t sfn[2] = {0, 0};    // SEP: S issues per lane (S-free waits)
             bool ok = true;
@@ -501,11 +518,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const int u = unit_of(p, cta, G, r);
                 if (u >= p.n_units) continue;
                 const Unit U = make_unit<PAIR>(p, u);
+                const int qb = C::NQB == 2 ? static_cast<int>(nunit & 1u) : 0;
+                ++nunit;
 #pragma unroll
                 for (int w = 0; w < C::NQ; ++w) {
                     if (!ok || U.qt[w] < 0) continue;
-                    ok = wait_warp(bar(C::B_QFULL + w), qn[w] & 1u, kSiteQFull);
-                    ++qn[w];
+                    ok = wait_warp(bar(C::B_QFULL + qb * C::NQ + w), (qpar >> (qb * C::NQ + w)) & 1u, kSiteQFull);
+                    qpar ^= 1u << (qb * C::NQ + w);
                 }
                 if (!ok) break;
                 tc_fence_after();
@@ -535,8 +554,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     for (int j = U.ulo; j < U.uhi && ok; ++j) {
                         const bool use0 = lane_uses(U, 0, j), use1 = lane_uses(U, 1, j);
                         if (!use0 && !use1) continue;
-                        const uint32_t kpos = rc, vpos = rc + 1;
-                        rc += 2;
+                        const uint32_t kpos = rc, vpos = rc + C::EPT;   // EPT = 1 here
+                        rc += 2 * C::EPT;
                         const uint32_t kslot = kpos % C::RING;
                         ok = wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
                                        kSiteKvFullK);
@@ -549,9 +568,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             if (!ok) break;
                             ++sfn[w];
                             tc_fence_after();
-                            issue_s(w, w, kslot);
+                            issue_s(qb * C::NQ + w, w, kslot);
                             mma_commit(bar(C::B_SFULL + w));
-                            if (j == U.hi[w] - 1) mma_commit(bar(C::B_QEMPTY + w));
+                            if (j == U.hi[w] - 1) mma_commit(bar(C::B_QEMPTY + qb * C::NQ + w));
                         }
                         if (!ok) break;
                         mma_commit(bar(C::B_KVEMPTY + kslot));
@@ -587,8 +606,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     for (int j = U.ulo; j < U.uhi && ok; ++j) {
                         const bool use0 = lane_uses(U, 0, j), use1 = lane_uses(U, 1, j);
                         if (!use0 && !use1) continue;
-                        const uint32_t kpos = rc, vpos = rc + 1;
-                        rc += 2;
+                        const uint32_t kpos = rc, vpos = rc + C::EPT;   // EPT = 1 here
+                        rc += 2 * C::EPT;
                         const uint32_t kslot = kpos % C::RING;
                         ok = wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
                                        kSiteKvFullK);
@@ -599,9 +618,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             if (!ok || !(w == 0 ? use0 : use1)) continue;
                             if (pend_j[w] >= 0) ok = flush_pv(w);
                             if (!ok) break;
-                            issue_s(w, w, kslot);
+                            issue_s(qb * C::NQ + w, w, kslot);
                             mma_commit(bar(C::B_SFULL + w));
-                            if (j == U.hi[w] - 1) mma_commit(bar(C::B_QEMPTY + w));
+                            if (j == U.hi[w] - 1) mma_commit(bar(C::B_QEMPTY + qb * C::NQ + w));
                             pend_j[w] = j;
                             pend_v[w] = vpos;
                         }
@@ -612,20 +631,40 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (ok && pend_j[w] >= 0) ok = flush_pv(w);
                 } else {
                     // One query tile, S buffers alternate: S(0), S(1), PV(0), S(2), PV(1), ...
+                    // A tile's K and V each come as EPT ring entries (head-dim parts):
+                    // S takes the k-steps of each K entry in turn; P.V is split along
+                    // N into one MMA chain per V entry.
+                    constexpr int KS_PER_ENTRY = 4 * C::ENTRY_CHUNKS;          // k-steps
+                    constexpr int NV = D / C::EPT;                             // N per part
+                    constexpr uint32_t IDESC_PVE = idesc_f16_f32acc(BF16, BM, NV, true);
                     const int n = U.hi[0] - U.lo[0];
                     const uint32_t base = rc;
-                    rc += 2u * static_cast<uint32_t>(n);
+                    rc += 2u * C::EPT * static_cast<uint32_t>(n);
                     auto do_s = [&](int t) -> bool {
-                        const uint32_t kpos = base + 2u * t;
-                        const uint32_t kslot = kpos % C::RING;
-                        if (!wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
-                                       kSiteKvFullK))
-                            return false;
-                        tc_fence_after();
-                        issue_s(0, t & 1, kslot);
+                        const uint32_t kpos = base + 2u * C::EPT * t;
+                        const uint64_t qd = sdesc_sw128(q_smem + qb * C::NQ * C::TILE_BYTES, 16, 1024);
+                        const uint32_t d_tmem = tmem + C::s_col(t & 1);
+#pragma unroll
+                        for (int e = 0; e < C::EPT; ++e) {
+                            const uint32_t kslot = (kpos + e) % C::RING;
+                            if (!wait_warp(bar(C::B_KVFULL + kslot), ((kpos + e) / C::RING) & 1u,
+                                           kSiteKvFullK))
+                                return false;
+                            tc_fence_after();
+                            const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::ENTRY_BYTES, 16, 1024);
+#pragma unroll
+                            for (int kl = 0; kl < KS_PER_ENTRY; ++kl) {
+                                const int kk = e * KS_PER_ENTRY + kl;
+                                const uint64_t qoff = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
+                                const uint64_t koff = (kl >> 2) * (C::CHUNK_BYTES >> 4) + (kl & 3) * 2;
+                                mma_ss(d_tmem, qd + qoff, kd + koff, IDESC_S, kk > 0 ? 1u : 0u);
+                            }
+                        }
                         mma_commit(bar(C::B_SFULL + (t & 1)));
-                        mma_commit(bar(C::B_KVEMPTY + kslot));
-                        if (t == n - 1) mma_commit(bar(C::B_QEMPTY + 0));
+#pragma unroll
+                        for (int e = 0; e < C::EPT; ++e)
+                            mma_commit(bar(C::B_KVEMPTY + (kpos + e) % C::RING));
+                        if (t == n - 1) mma_commit(bar(C::B_QEMPTY + qb * C::NQ));
                         return true;
                     };
                     ok = do_s(0);
@@ -636,15 +675,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         ok = wait_warp(bar(C::B_PFULL + b), pn[b] & 1u, kSitePFull);
                         if (!ok) break;
                         ++pn[b];
-                        const uint32_t vpos = base + 2u * t + 1u;
-                        const uint32_t vslot = vpos % C::RING;
-                        ok = wait_warp(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u,
-                                       kSiteKvFullV);
+                        const uint32_t vpos = base + 2u * C::EPT * t + C::EPT;
+#pragma unroll
+                        for (int e = 0; e < C::EPT; ++e) {
+                            if (!ok) continue;
+                            const uint32_t vslot = (vpos + e) % C::RING;
+                            ok = wait_warp(bar(C::B_KVFULL + vslot), ((vpos + e) / C::RING) & 1u,
+                                           kSiteKvFullV);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES,
+                                                            C::CHUNK_BYTES, 1024);
+                            const uint32_t d_tmem = tmem + C::o_col(0) + e * NV;
+                            const uint32_t a_tmem = tmem + C::p_col(b);
+#pragma unroll
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128),
+                                       IDESC_PVE, (t > 0 || kk > 0) ? 1u : 0u);
+                        }
                         if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(b, 0, vslot, t > 0);
                         mma_commit(bar(C::B_ODONE + b));
-                        mma_commit(bar(C::B_KVEMPTY + vslot));
+#pragma unroll
+                        for (int e = 0; e < C::EPT; ++e)
+                            mma_commit(bar(C::B_KVEMPTY + (vpos + e) % C::RING));
                     }
                 }
             }
@@ -698,8 +751,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             }
             float m_ref = -INFINITY;                    // running max (log2 units, may lag)
             float l = 0.f;                              // running denominator
-            int t = 0;
-            for (int j = j_lo; j < j_hi && ok; ++j, ++t) {
+            for (int t = 0; t < j_hi - j_lo && ok; ++t) {
+                const int j = j_lo + t;
                 const int b = PAIR ? wg : (t & 1);
                 ok = wait_warp(bar(C::B_SFULL + b), sn.get(b) & 1u, kSiteSFull);
                 if (!ok) break;
@@ -718,11 +771,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
                     tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
                     tmem_wait_ld();
+                    // the upper half loads while the lower half is reduced
+                    tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                    tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
                     if (masked) mask_half(lo, 0, rel_lo, rel_hi, fill);
                     ext = row_extreme64(lo, sc >= 0.f);
                 }
-                tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
-                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
                 tmem_wait_ld();
                 if (masked) mask_half(hi, 64, rel_lo, rel_hi, fill);
                 {
@@ -749,6 +803,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         tc_fence_after();
                     }
                 }
+
                 // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
                 // upper half of the S columns: the upper 64 keys first (their S
                 // columns are already in registers), then the lower 64 keys,
@@ -777,6 +832,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     else
                         exp_half<BF16, false, C::EMU>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
                 }
+
                 acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
                 l = l * alpha + (acc[0].x + acc[0].y);
 
