@@ -82,8 +82,6 @@ struct Cfg {
     static constexpr int ENTRY_BYTES = TILE_BYTES / EPT;
     static constexpr int ENTRY_CHUNKS = CHUNKS / EPT;
     static constexpr int RING = D == 64 ? 8 : 5;
-    // pairs of every 8 whose exp2 runs on the FMA pipe (see exp2_emu2)
-    static constexpr int EMU = 0;
     static constexpr int NUM_WARPS = 4 * NWG + 2;
     static constexpr int THREADS = 32 * NUM_WARPS;
     static constexpr int WARP_TMA = 4 * NWG;
@@ -292,29 +290,7 @@ __device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool wan
 // packed fma, MUFU ex2, packed partial sums into acc[8], rounding to 16-bit
 // pairs and one 32-column TMEM store at `dst`.  The packed fp32x2 builtins
 // let the compiler keep operand pairs in register pairs.
-// exp2 of a pair on the FMA pipe instead of the MUFU: 2^x = 2^j * 2^f with
-// j = round(x) (left in the low mantissa bits of x + 1.5*2^23) and
-// f = x - j in [-1/2, 1/2]; 2^f is a degree-3 polynomial with minimal
-// maximum relative error on [-1/2, 1/2] (Remez exchange, coefficients from
-// fit_exp2_poly.py next to this file); relative error of the fp32 evaluation
-// below 7.5e-5, well under the rounding of P to 16 bits.  x is clamped at
-// -125 so that 2^j stays a normal number (such a p is 0 after rounding anyway).
-__device__ __forceinline__ float2 exp2_emu2(float2 x) {
-    constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
-    constexpr float c0 = 0.999928057f, c1 = 0.693260968f, c2 = 0.242611125f, c3 = 0.0551716685f;
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
-    const float2 j = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
-    const float2 f = __ffma2_rn(j, make_float2(-1.f, -1.f), x);
-    float2 q = __ffma2_rn(make_float2(c3, c3), f, make_float2(c2, c2));
-    q = __ffma2_rn(q, f, make_float2(c1, c1));
-    q = __ffma2_rn(q, f, make_float2(c0, c0));
-    return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
-}
-
-template <bool BF16, bool MASKED, int EMU>
+template <bool BF16, bool MASKED>
 __device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, int rel_lo, int rel_hi,
                                          float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
     const float2 sc2 = make_float2(sc, sc);
@@ -324,13 +300,7 @@ __device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, int 
     for (int e = 0; e < 32; ++e) {
         const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
                                     sc2, nm2);
-        // EMU of every 8 pairs go through the FMA-pipe polynomial, the rest
-        // through the MUFU, to balance the two pipes
-        float2 pp;
-        if ((e & 7) < EMU)
-            pp = exp2_emu2(x);
-        else
-            pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if constexpr (MASKED) {
             const unsigned width = static_cast<unsigned>(rel_hi - rel_lo);
             const int c0 = base + 2 * e;
@@ -813,9 +783,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // (the element-wise mask exists only in the masked instantiation,
                 // chosen once per tile)
                 if (masked)
-                    exp_half<BF16, true, C::EMU>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                    exp_half<BF16, true>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
                 else
-                    exp_half<BF16, false, C::EMU>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                    exp_half<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
                 {
                     uint32_t lo[64];
                     tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
@@ -828,9 +798,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
                     }
                     if (masked)
-                        exp_half<BF16, true, C::EMU>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                        exp_half<BF16, true>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
                     else
-                        exp_half<BF16, false, C::EMU>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                        exp_half<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
                 }
 
                 acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));

@@ -52,6 +52,9 @@ def parse_args():
                     help="skip the per-mask-kind measurements of the other workloads")
     ap.add_argument("--soak-s", type=float, default=2.0,
                     help="seconds of untimed launches before the timed region (clock sampling)")
+    ap.add_argument("--lean", action="store_true",
+                    help="only the device-timed line: no soak, e2e, CPU baseline or other "
+                         "workloads (for profiler runs)")
     return ap.parse_args()
 
 
@@ -357,7 +360,9 @@ def main():
 
     peaks, peaks_kind = load_peaks()
     flops, nbytes = af.work(w.B, w.H, w.L, w.D, w.mask, w.block_size, w.dtype)
-    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if args.lean:
+        args.soak_s, args.no_all = 0.0, True
+    sampler = ClockSampler(dev.index) if rank == 0 and not args.lean else None
     ms, info = time_workload(af, w, dev, args.steps, args.warmup, soak_s=args.soak_s,
                              sampler=sampler, dist=dist)
     clocks = sampler.stop() if sampler else None
@@ -365,8 +370,10 @@ def main():
 
     if dist:
         dist.barrier()
-    e2e_s, h2d, d2h = time_e2e(af, w, dev, max(10, min(args.steps, 200)), 3)
-    e2e_s = reduce_max(e2e_s, dist, dev)
+    e2e_s, h2d, d2h = (None, 0, 0) if args.lean else \
+        time_e2e(af, w, dev, max(10, min(args.steps, 200)), 3)
+    if e2e_s is not None:
+        e2e_s = reduce_max(e2e_s, dist, dev)
 
     per_mask = {}
     if not args.no_all:
@@ -404,14 +411,15 @@ def main():
         "dtype": "f16" if w.dtype == torch.float16 else "bf16", "data": "synthetic",
         "config": cfg,
         "roofline": roofline_for(w, flops, nbytes, ms, peaks, peaks_kind, ncu_traffic(w.name)),
-        "e2e": {"value": round(job_tflops(flops, world, e2e_s * 1e3), 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "e2e": None if e2e_s is None else {
+            "value": round(job_tflops(flops, world, e2e_s * 1e3), 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "per_workload": per_mask or None,
     }
-    out["cpu_baseline"] = cpu_baseline(w)
+    out["cpu_baseline"] = None if args.lean else cpu_baseline(w)
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
