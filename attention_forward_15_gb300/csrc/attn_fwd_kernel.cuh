@@ -89,6 +89,9 @@ struct Cfg {
     // SEP: P has columns of its own (D = 64 leaves room), so the next S of a
     // lane can be computed while the softmax still works on the current one.
     static constexpr bool SEP = PAIR && D == 64;
+    // ROW_IN_REGS: the softmax holds a whole 128-key S row in registers (one TMEM
+    // round trip per tile); only the single mode has the registers for it.
+    static constexpr bool ROW_IN_REGS = !PAIR;
     // TMEM columns of S buffer b, of P buffer b and of the O accumulator of lane w.
     // Without SEP, P (16-bit pairs) occupies the upper BN/2 columns of its S.
     __device__ static constexpr uint32_t s_col(int b) { return static_cast<uint32_t>(b) * 128u; }
@@ -311,6 +314,34 @@ __device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, int 
         pk[e] = pack2<BF16>(pp.x, pp.y);
     }
     tmem_st32(dst, pk);
+}
+
+// p = exp2(s * sc - m) for a 32-key chunk (keys base..base+31 of the tile):
+// packed fma, MUFU ex2, packed partial sums into acc[4], rounding to 16-bit
+// pairs and one 16-column TMEM store at `dst`.  The packed fp32x2 builtins
+// let the compiler keep operand pairs in register pairs; the element-wise mask
+// exists only in the masked instantiation, which is chosen once per tile.
+template <bool BF16, bool MASKED>
+__device__ __forceinline__ void exp_chunk(const uint32_t *v, int base, int rel_lo, int rel_hi,
+                                          float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(neg_m, neg_m);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                    sc2, nm2);
+        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if constexpr (MASKED) {
+            const unsigned width = static_cast<unsigned>(rel_hi - rel_lo);
+            const int c0 = base + 2 * e;
+            if (static_cast<unsigned>(c0 - rel_lo) >= width) pp.x = 0.f;
+            if (static_cast<unsigned>(c0 + 1 - rel_lo) >= width) pp.y = 0.f;
+        }
+        acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
+        pk[e] = pack2<BF16>(pp.x, pp.y);
+    }
+    tmem_st16(dst, pk);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -732,77 +763,136 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const uint32_t p_addr = tmem + lane_off + C::p_col(b);
                 const bool masked = tile_masked(p, qt, j);
                 const int rel_lo = klo - j * BN, rel_hi = khi - j * BN;
-                // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
-                // two 64-key halves; the upper half stays in registers.
-                uint32_t hi[64];
-                float ext;
-                {
-                    uint32_t lo[64];
-                    tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
-                    tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
-                    tmem_wait_ld();
-                    // the upper half loads while the lower half is reduced
-                    tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
-                    tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
-                    if (masked) mask_half(lo, 0, rel_lo, rel_hi, fill);
-                    ext = row_extreme64(lo, sc >= 0.f);
-                }
-                tmem_wait_ld();
-                if (masked) mask_half(hi, 64, rel_lo, rel_hi, fill);
-                {
-                    const float e2 = row_extreme64(hi, sc >= 0.f);
-                    ext = sc >= 0.f ? fmaxf(ext, e2) : fminf(ext, e2);
-                }
-                const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
-                float alpha = 1.f;
-                bool rescale = false;
-                if (t == 0) {
-                    m_ref = m_tile;
-                } else if (m_tile > m_ref + kRescaleLog2) {
-                    alpha = ex2_approx(m_ref - m_tile);
-                    m_ref = m_tile;
-                    rescale = true;
-                }
-                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                if constexpr (C::SEP) {
-                    // P and O of this lane are still read/written by the previous
-                    // tile's P.V until it completes.
-                    if (t > 0) {
-                        ok = wait_pv(wg);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                }
-
-                // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
-                // upper half of the S columns: the upper 64 keys first (their S
-                // columns are already in registers), then the lower 64 keys,
-                // reloaded (their P columns overwrite S columns 64..95, consumed).
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
-                // (the element-wise mask exists only in the masked instantiation,
-                // chosen once per tile)
-                if (masked)
-                    exp_half<BF16, true>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
-                else
-                    exp_half<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
-                {
-                    uint32_t lo[64];
-                    tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
-                    tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                float alpha = 1.f;
+                bool rescale = false;
+                float neg_m = 0.f;
+                if constexpr (C::ROW_IN_REGS) {
+                    // Pass 1: the whole S row into registers (one TMEM round trip), then
+                    // its extreme (max for sm_scale >= 0, else min).
+                    uint32_t sv[BN];
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+                        tmem_ld32(s_addr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
                     tmem_wait_ld();
                     if constexpr (C::SEP) {
-                        // last read of this S: the MMA warp may overwrite it now
+                        // S is read: the MMA warp may overwrite it with the next tile
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
                     }
-                    if (masked)
-                        exp_half<BF16, true>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
-                    else
-                        exp_half<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
-                }
+                    if (masked) {
+                        mask_half(*reinterpret_cast<uint32_t(*)[64]>(sv), 0, rel_lo, rel_hi, fill);
+                        mask_half(*reinterpret_cast<uint32_t(*)[64]>(sv + 64), 64, rel_lo, rel_hi, fill);
+                    }
+                    float ext;
+                    {
+                        const float e1 = row_extreme64(*reinterpret_cast<const uint32_t(*)[64]>(sv), sc >= 0.f);
+                        const float e2 = row_extreme64(*reinterpret_cast<const uint32_t(*)[64]>(sv + 64), sc >= 0.f);
+                        ext = sc >= 0.f ? fmaxf(e1, e2) : fminf(e1, e2);
+                    }
+                    const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
+                    if (t == 0) {
+                        m_ref = m_tile;
+                    } else if (m_tile > m_ref + kRescaleLog2) {
+                        alpha = ex2_approx(m_ref - m_tile);
+                        m_ref = m_tile;
+                        rescale = true;
+                    }
+                    neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                    if constexpr (C::SEP) {
+                        // P and O of this lane are still read/written by the previous
+                        // tile's P.V until it completes.
+                        if (t > 0) {
+                            ok = wait_pv(wg);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                    }
+                    // Pass 2: P = exp2(s*scale - m) in 32-key chunks, rounded to 16-bit
+                    // pairs and written to the P columns (without SEP: the upper half
+                    // of this S, whose values are already in registers).
+                    if (masked) {
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c)
+                            exp_chunk<BF16, true>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc,
+                                                  p_addr + 16 * c);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c)
+                            exp_chunk<BF16, false>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc,
+                                                   p_addr + 16 * c);
+                    }
+                } else {
+                    // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
+                    // two 64-key halves; the upper half stays in registers.
+                    uint32_t hi[64];
+                    float ext;
+                    {
+                        uint32_t lo[64];
+                        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                        tmem_wait_ld();
+                        // the upper half loads while the lower half is reduced
+                        tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                        tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
+                        if (masked) mask_half(lo, 0, rel_lo, rel_hi, fill);
+                        ext = row_extreme64(lo, sc >= 0.f);
+                    }
+                    tmem_wait_ld();
+                    if (masked) mask_half(hi, 64, rel_lo, rel_hi, fill);
+                    {
+                        const float e2 = row_extreme64(hi, sc >= 0.f);
+                        ext = sc >= 0.f ? fmaxf(ext, e2) : fminf(ext, e2);
+                    }
+                    const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
+                    if (t == 0) {
+                        m_ref = m_tile;
+                    } else if (m_tile > m_ref + kRescaleLog2) {
+                        alpha = ex2_approx(m_ref - m_tile);
+                        m_ref = m_tile;
+                        rescale = true;
+                    }
+                    neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                    if constexpr (C::SEP) {
+                        // P and O of this lane are still read/written by the previous
+                        // tile's P.V until it completes.
+                        if (t > 0) {
+                            ok = wait_pv(wg);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                    }
 
+                    // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
+                    // upper half of the S columns: the upper 64 keys first (their S
+                    // columns are already in registers), then the lower 64 keys,
+                    // reloaded (their P columns overwrite S columns 64..95, consumed).
+                    // (the element-wise mask exists only in the masked instantiation,
+                    // chosen once per tile)
+                    if (masked)
+                        exp_half<BF16, true>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                    else
+                        exp_half<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                    {
+                        uint32_t lo[64];
+                        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                        tmem_wait_ld();
+                        if constexpr (C::SEP) {
+                            // last read of this S: the MMA warp may overwrite it now
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
+                        }
+                        if (masked)
+                            exp_half<BF16, true>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                        else
+                            exp_half<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                    }
+
+                }
                 acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
                 l = l * alpha + (acc[0].x + acc[0].y);
 
