@@ -28,6 +28,7 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+int g_inject = 0;   // fault-injection mode for the next attn_fwd calls (tests only)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int head_dim_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : (D == 256 ? 2 : -1)); }
@@ -160,6 +161,12 @@ extern "C" {
 
 int attn_abi_version(void) { return (1 << 16) | 0; }
 
+int attn_debug_inject(int mode) {
+    if (mode != 0 && mode != 1) return ATTN_ERR_ARG;
+    g_inject = mode;
+    return ATTN_OK;
+}
+
 const char *attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
@@ -239,6 +246,7 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     prm.n_kv = pl.n_kv;
     prm.n_units = pl.n_units;
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
+    prm.inject = g_inject;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == ATTN_BF16;
@@ -366,6 +374,7 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, voi
     prm.n_kv = pl.n_kv;
     prm.n_units = pl.n_units;
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
+    prm.inject = 0;
 
     const bool bf16 = dtype == ATTN_BF16;
     switch (D) {

@@ -67,6 +67,8 @@ struct FwdParams {
     int n_qt, n_kv;          // query / key tiles per head
     int n_units;
     float scale_log2;        // sm_scale * log2(e)
+    int inject;              // test hook: 1 = the producer issues no copies, so every
+                             // consumer's bounded wait runs out (0 in normal use)
 };
 
 template <int D, bool PAIR>
@@ -422,7 +424,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             uint32_t qpar = 0;           // bit q: parity of the loads into Q slot q
             uint32_t qused = 0;          // bit q: Q slot q has been loaded
             uint32_t nunit = 0;          // units of this CTA so far
-            bool ok = true;
+            bool ok = p.inject != 1;
             for (int r = 0; r < rounds && ok; ++r) {
                 const int u = unit_of(p, cta, G, r);
                 if (u >= p.n_units) continue;

@@ -149,6 +149,16 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
 int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size,
                   int dtype, int *units, int *ctas, int *threads, int *smem_bytes);
 
+/*
+ * attn_debug_inject -- TEST HOOK, not for production use.  mode 1 makes every
+ * following attn_fwd launch start with its copy-issuing warp doing nothing, so
+ * each consumer's bounded wait runs out after about one second: the kernel
+ * records ATTN_ERR_TIMEOUT in the device status word, frees its tensor memory
+ * and returns (outputs undefined), without hanging the GPU.  mode 0 restores
+ * normal operation.  Process-wide, not thread-safe; attn_fwd_noalloc ignores it.
+ */
+int attn_debug_inject(int mode);
+
 /* ABI version of this header: (major << 16) | minor. */
 int attn_abi_version(void);
 

@@ -128,7 +128,7 @@ def test_unusual_scales(af, scale):
     _full_case(af, 1, 2, 256, 64, BLOCK_DIAG, 32, torch.float16, scale=scale)
 
 
-@pytest.mark.parametrize("case", PAGE_TEST_MATRIX[:6], ids=str)
+@pytest.mark.parametrize("case", PAGE_TEST_MATRIX, ids=str)
 @pytest.mark.parametrize("causal", [False, True])
 def test_page_test_matrix(af, case, causal):
     """The Fused Attention page's test shapes (seed 20, N(0, 0.5), sm_scale 0.5),
