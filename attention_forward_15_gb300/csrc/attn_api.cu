@@ -69,6 +69,12 @@ Plan make_plan(int B, int H, int L, int D) {
     return pl;
 }
 
+// K and V of the whole problem comfortably inside the 129 MB L2: every query
+// tile of a head re-reads its K/V, so asking L2 to keep them pays.
+bool kv_fits_l2(int BH, int L, int D) {
+    return 2.0 * BH * static_cast<double>(L) * D * 2.0 <= 64.0 * 1024 * 1024;
+}
+
 int threads_for(int D) { return D <= 128 ? Cfg<64, true>::THREADS : Cfg<256, false>::THREADS; }
 
 int smem_for(int D) {
@@ -247,6 +253,7 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     prm.n_units = pl.n_units;
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
     prm.inject = g_inject;
+    prm.kv_keep = kv_fits_l2(prm.BH, L, D) ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == ATTN_BF16;
@@ -375,6 +382,7 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, voi
     prm.n_units = pl.n_units;
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
     prm.inject = 0;
+    prm.kv_keep = kv_fits_l2(prm.BH, L, D) ? 1 : 0;
 
     const bool bf16 = dtype == ATTN_BF16;
     switch (D) {

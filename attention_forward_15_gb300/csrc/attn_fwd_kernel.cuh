@@ -67,6 +67,7 @@ struct FwdParams {
     int n_qt, n_kv;          // query / key tiles per head
     int n_units;
     float scale_log2;        // sm_scale * log2(e)
+    int kv_keep;             // 1: K/V loads ask L2 to keep them (all K/V fit in L2)
     int inject;              // test hook: 1 = the producer issues no copies, so every
                              // consumer's bounded wait runs out (0 in normal use)
 };
@@ -458,9 +459,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::ENTRY_BYTES);
                         const uint32_t dst = s_base + C::OFF_RING + slot * C::ENTRY_BYTES;
                         const CUtensorMap *m = kind == 0 ? &tmap_k : &tmap_v;
-                        for (int c = 0; c < C::ENTRY_CHUNKS; ++c)
-                            tma_load_3d(dst + c * C::CHUNK_BYTES, m, (e * C::ENTRY_CHUNKS + c) * 64,
-                                        j * BN, U.bh, bar(C::B_KVFULL + slot));
+                        for (int c = 0; c < C::ENTRY_CHUNKS; ++c) {
+                            if (p.kv_keep)
+                                tma_load_3d_keep(dst + c * C::CHUNK_BYTES, m,
+                                                 (e * C::ENTRY_CHUNKS + c) * 64, j * BN, U.bh,
+                                                 bar(C::B_KVFULL + slot));
+                            else
+                                tma_load_3d(dst + c * C::CHUNK_BYTES, m, (e * C::ENTRY_CHUNKS + c) * 64,
+                                            j * BN, U.bh, bar(C::B_KVFULL + slot));
+                        }
                         ++rc;
                     }
                 }
