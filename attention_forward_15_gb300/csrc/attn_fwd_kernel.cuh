@@ -85,13 +85,16 @@ struct Cfg {
     static constexpr int ENTRY_BYTES = TILE_BYTES / EPT;
     static constexpr int ENTRY_CHUNKS = CHUNKS / EPT;
     static constexpr int RING = D == 64 ? 8 : 5;
-    static constexpr int NUM_WARPS = 4 * NWG + 2;
+    // SEP: P has columns of its own (D = 64 leaves room), so the next S of a
+    // lane can be computed while the softmax still works on the current one.
+    // Then a second MMA warp issues the P.V products, so that neither issuer's
+    // barrier waits hold back the other's MMAs.
+    static constexpr bool SEP = PAIR && D == 64;
+    static constexpr int NUM_WARPS = 4 * NWG + 2 + (SEP ? 1 : 0);
     static constexpr int THREADS = 32 * NUM_WARPS;
     static constexpr int WARP_TMA = 4 * NWG;
     static constexpr int WARP_MMA = 4 * NWG + 1;
-    // SEP: P has columns of its own (D = 64 leaves room), so the next S of a
-    // lane can be computed while the softmax still works on the current one.
-    static constexpr bool SEP = PAIR && D == 64;
+    static constexpr int WARP_PV = 4 * NWG + 2;     // SEP only
     // ROW_IN_REGS: the softmax holds a whole 128-key S row in registers (one TMEM
     // round trip per tile); only the single mode has the registers for it.
     static constexpr bool ROW_IN_REGS = !PAIR;
@@ -385,7 +388,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(C::B_ODONE + b), 1);
             mbar_init(bar(C::B_SFREE + b), 4);   // one arrival per softmax warp
         }
-        mbar_init(bar(C::B_DRAIN), 1);
+        mbar_init(bar(C::B_DRAIN), C::SEP ? 2 : 1);   // one commit per MMA-issuing warp
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -416,6 +419,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     };
 
     const int rounds = tmem_ok ? rounds_all : 0;
+
+    // MMA issue helpers (called by a whole converged warp; one elected lane issues)
+        constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
+        constexpr uint32_t IDESC_PV = idesc_f16_f32acc(BF16, BM, D, true);
+        const uint32_t q_smem = s_base + C::OFF_Q;
+        const uint32_t ring_smem = s_base + C::OFF_RING;
+        // Descriptors advance by adding to their 16-byte-unit address field.
+        // S = Q K^T: k-step kk covers head-dim columns [16kk, 16kk+16): box kk/4,
+        // 32-byte offset (kk%4) inside the 128-byte swizzled row.
+        auto issue_s = [&](int qslot, int sbuf, uint32_t kslot) {
+            const uint64_t qd = sdesc_sw128(q_smem + qslot * C::TILE_BYTES, 16, 1024);
+            const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::ENTRY_BYTES, 16, 1024);
+            const uint32_t d_tmem = tmem + C::s_col(sbuf);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
+                mma_ss(d_tmem, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+        };
+        // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
+        // consecutive 64-column boxes of V are C::CHUNK_BYTES apart (LBO).
+        auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
+            const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, C::CHUNK_BYTES, 1024);
+            const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
+            const uint32_t a_tmem = tmem + C::p_col(sbuf);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
+                       (accumulate || kk > 0) ? 1u : 0u);
+        };
 
     if (warp == C::WARP_TMA) {
         // ================================================================ TMA producer
@@ -489,35 +522,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         // (the whole warp runs this loop; one elected lane -- always the same
         // one, so its commits cover its MMAs -- issues each tcgen05 instruction)
         {
-            constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
-            constexpr uint32_t IDESC_PV = idesc_f16_f32acc(BF16, BM, D, true);
-            const uint32_t q_smem = s_base + C::OFF_Q;
-            const uint32_t ring_smem = s_base + C::OFF_RING;
-            // Descriptors advance by adding to their 16-byte-unit address field.
-            // S = Q K^T: k-step kk covers head-dim columns [16kk, 16kk+16): box kk/4,
-            // 32-byte offset (kk%4) inside the 128-byte swizzled row.
-            auto issue_s = [&](int qslot, int sbuf, uint32_t kslot) {
-                const uint64_t qd = sdesc_sw128(q_smem + qslot * C::TILE_BYTES, 16, 1024);
-                const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::ENTRY_BYTES, 16, 1024);
-                const uint32_t d_tmem = tmem + C::s_col(sbuf);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
-                    mma_ss(d_tmem, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
-                }
-            };
-            // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
-            // consecutive 64-column boxes of V are C::CHUNK_BYTES apart (LBO).
-            auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
-                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, C::CHUNK_BYTES, 1024);
-                const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
-                const uint32_t a_tmem = tmem + C::p_col(sbuf);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
-                           (accumulate || kk > 0) ? 1u : 0u);
-            };
-
             uint32_t rc = 0;
             uint32_t qpar = 0;           // bit q: parity of the Q-full waits of slot q
             uint32_t nunit = 0;
@@ -539,33 +543,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (!ok) break;
                 tc_fence_after();
                 if constexpr (C::SEP) {
-                    // Per key tile: S of both lanes as soon as their softmax has read
-                    // the previous S, then the P.V of the previous tiles as their P
-                    // arrives.  A lane's P.V(t) is issued after its S(t+1).
-                    int pend_j[2] = {-1, -1};
-                    uint32_t pend_v[2] = {0, 0};
-                    int npv[2] = {0, 0};
-                    auto flush_pv = [&](int w) -> bool {
-                        if (!wait_warp(bar(C::B_PFULL + w), pn[w] & 1u, kSitePFull)) return false;
-                        ++pn[w];
-                        const uint32_t vslot = pend_v[w] % C::RING;
-                        if (!wait_warp(bar(C::B_KVFULL + vslot), (pend_v[w] / C::RING) & 1u,
-                                       kSiteKvFullV))
-                            return false;
-                        tc_fence_after();
-                        issue_pv(w, w, vslot, npv[w] > 0);
-                        ++npv[w];
-                        mma_commit(bar(C::B_ODONE + w));
-                        const bool other_needs = pend_j[1 - w] == pend_j[w];
-                        pend_j[w] = -1;
-                        if (!other_needs) mma_commit(bar(C::B_KVEMPTY + vslot));
-                        return true;
-                    };
+                    // Per key tile: S(t+1) of each lane as soon as its softmax has
+                    // read S(t); the P.V products are the other MMA warp's.
                     for (int j = U.ulo; j < U.uhi && ok; ++j) {
                         const bool use0 = lane_uses(U, 0, j), use1 = lane_uses(U, 1, j);
                         if (!use0 && !use1) continue;
-                        const uint32_t kpos = rc, vpos = rc + C::EPT;   // EPT = 1 here
-                        rc += 2 * C::EPT;
+                        const uint32_t kpos = rc;
+                        rc += 2;                                        // K and V entries
                         const uint32_t kslot = kpos % C::RING;
                         ok = wait_warp(bar(C::B_KVFULL + kslot), (kpos / C::RING) & 1u,
                                        kSiteKvFullK);
@@ -584,15 +568,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         }
                         if (!ok) break;
                         mma_commit(bar(C::B_KVEMPTY + kslot));
-#pragma unroll
-                        for (int w = 0; w < 2; ++w)
-                            if (ok && pend_j[w] >= 0) ok = flush_pv(w);
-                        if (use0) { pend_j[0] = j; pend_v[0] = vpos; }
-                        if (use1) { pend_j[1] = j; pend_v[1] = vpos; }
                     }
-#pragma unroll
-                    for (int w = 0; w < 2; ++w)
-                        if (ok && pend_j[w] >= 0) ok = flush_pv(w);
                 } else if constexpr (PAIR) {
                     int pend_j[2] = {-1, -1};
                     uint32_t pend_v[2] = {0, 0};
@@ -717,6 +693,50 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             wait_slow(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
         }
         __syncwarp();
+    } else if (C::SEP && warp == C::WARP_PV) {
+        // ================================================================ P.V issuer
+        // (separate-P pair mode; whole warp converged, one elected lane issues):
+        // O_w += P_w V for each lane as soon as its P arrives, lane 0 first.
+        {
+            uint32_t rc = 0;
+            uint32_t pn[2] = {0, 0};     // P-ready waits per lane
+            bool ok = true;
+            for (int r = 0; r < rounds && ok; ++r) {
+                const int u = unit_of(p, cta, G, r);
+                if (u >= p.n_units) continue;
+                const Unit U = make_unit<PAIR>(p, u);
+                int npv[2] = {0, 0};
+                for (int j = U.ulo; j < U.uhi && ok; ++j) {
+                    const bool use0 = lane_uses(U, 0, j), use1 = lane_uses(U, 1, j);
+                    if (!use0 && !use1) continue;
+                    const uint32_t vpos = rc + 1;
+                    rc += 2;                                            // K and V entries
+                    const uint32_t vslot = vpos % C::RING;
+                    bool v_ready = false;
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        if (!ok || !(w == 0 ? use0 : use1)) continue;
+                        ok = wait_warp(bar(C::B_PFULL + w), pn[w] & 1u, kSitePFull);
+                        if (!ok) break;
+                        ++pn[w];
+                        if (!v_ready) {
+                            ok = wait_warp(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u, kSiteKvFullV);
+                            if (!ok) break;
+                            v_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_pv(w, w, vslot, npv[w] > 0);
+                        ++npv[w];
+                        mma_commit(bar(C::B_ODONE + w));
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(C::B_KVEMPTY + vslot));
+                }
+            }
+            mma_commit(bar(C::B_DRAIN));
+            wait_slow(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
+        }
+        __syncwarp();
     } else {
         // ================================================================ softmax groups
         const int wg = warp >> 2;                       // lane (query tile slot) of this group
@@ -834,71 +854,123 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                                    p_addr + 16 * c);
                     }
                 } else {
-                    // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
-                    // two 64-key halves; the upper half stays in registers.
-                    uint32_t hi[64];
-                    float ext;
-                    {
-                        uint32_t lo[64];
-                        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
-                        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
-                        tmem_wait_ld();
-                        // the upper half loads while the lower half is reduced
-                        tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
-                        tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
-                        if (masked) mask_half(lo, 0, rel_lo, rel_hi, fill);
-                        ext = row_extreme64(lo, sc >= 0.f);
-                    }
-                    tmem_wait_ld();
-                    if (masked) mask_half(hi, 64, rel_lo, rel_hi, fill);
-                    {
-                        const float e2 = row_extreme64(hi, sc >= 0.f);
-                        ext = sc >= 0.f ? fmaxf(ext, e2) : fminf(ext, e2);
-                    }
-                    const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
-                    if (t == 0) {
-                        m_ref = m_tile;
-                    } else if (m_tile > m_ref + kRescaleLog2) {
-                        alpha = ex2_approx(m_ref - m_tile);
-                        m_ref = m_tile;
-                        rescale = true;
-                    }
-                    neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                    bool done = false;
                     if constexpr (C::SEP) {
-                        // P and O of this lane are still read/written by the previous
-                        // tile's P.V until it completes.
-                        if (t > 0) {
-                            ok = wait_pv(wg);
-                            if (!ok) break;
-                            tc_fence_after();
+                        // One pass against the running reference max.  S stays in TMEM
+                        // until this tile's S-free arrival (P has columns of its own),
+                        // so a tile whose scores climb more than the rescale threshold
+                        // above the reference is simply redone by the two-pass path
+                        // below; such tiles are rare once a row has seen a few keys.
+                        if (t > 0 && !masked) {
+                            uint32_t sv[64];
+                            tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                            tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                            tmem_wait_ld();
+                            const float lim = m_ref + kRescaleLog2;
+                            bool fits = m_ref != -INFINITY &&
+                                        row_extreme64(sv, sc >= 0.f) * sc <= lim;
+                            if (__all_sync(0xffffffffu, fits)) {
+                                // P and O of this lane are still read/written by the
+                                // previous tile's P.V until it completes.
+                                ok = wait_pv(wg);
+                                if (!ok) break;
+                                tc_fence_after();
+                                neg_m = -m_ref;
+                                // keys 0..63 from registers while keys 64..127 load
+                                exp_chunk<BF16, false>(sv, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                                tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                                exp_chunk<BF16, false>(sv + 32, 32, rel_lo, rel_hi, sc, neg_m, acc,
+                                                       p_addr + 16);
+                                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                                tmem_wait_ld();
+                                fits = row_extreme64(sv, sc >= 0.f) * sc <= lim;
+                                if (__all_sync(0xffffffffu, fits)) {
+                                    // last read of this S: the MMA warp may overwrite it now
+                                    tc_fence_before();
+                                    __syncwarp();
+                                    if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
+                                    exp_chunk<BF16, false>(sv, 64, rel_lo, rel_hi, sc, neg_m, acc,
+                                                           p_addr + 32);
+                                    exp_chunk<BF16, false>(sv + 32, 96, rel_lo, rel_hi, sc, neg_m, acc,
+                                                           p_addr + 48);
+                                    done = true;
+                                } else {
+                                    // redo the whole tile: forget the first half's sums and
+                                    // let its P stores land before they are overwritten
+                                    tmem_wait_st();
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
+                                }
+                            }
                         }
                     }
-
-                    // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
-                    // upper half of the S columns: the upper 64 keys first (their S
-                    // columns are already in registers), then the lower 64 keys,
-                    // reloaded (their P columns overwrite S columns 64..95, consumed).
-                    // (the element-wise mask exists only in the masked instantiation,
-                    // chosen once per tile)
-                    if (masked)
-                        exp_half<BF16, true>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
-                    else
-                        exp_half<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
-                    {
-                        uint32_t lo[64];
-                        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
-                        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
-                        tmem_wait_ld();
-                        if constexpr (C::SEP) {
-                            // last read of this S: the MMA warp may overwrite it now
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
+                    if (!done) {
+                        // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
+                        // two 64-key halves; the upper half stays in registers.
+                        uint32_t hi[64];
+                        float ext;
+                        {
+                            uint32_t lo[64];
+                            tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                            tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                            tmem_wait_ld();
+                            // the upper half loads while the lower half is reduced
+                            tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                            tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
+                            if (masked) mask_half(lo, 0, rel_lo, rel_hi, fill);
+                            ext = row_extreme64(lo, sc >= 0.f);
                         }
+                        tmem_wait_ld();
+                        if (masked) mask_half(hi, 64, rel_lo, rel_hi, fill);
+                        {
+                            const float e2 = row_extreme64(hi, sc >= 0.f);
+                            ext = sc >= 0.f ? fmaxf(ext, e2) : fminf(ext, e2);
+                        }
+                        const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
+                        if (t == 0) {
+                            m_ref = m_tile;
+                        } else if (m_tile > m_ref + kRescaleLog2) {
+                            alpha = ex2_approx(m_ref - m_tile);
+                            m_ref = m_tile;
+                            rescale = true;
+                        }
+                        neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                        if constexpr (C::SEP) {
+                            // P and O of this lane are still read/written by the previous
+                            // tile's P.V until it completes.
+                            if (t > 0) {
+                                ok = wait_pv(wg);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                        }
+
+                        // Pass 2: P = exp2(s*scale - m) written as 16-bit pairs into the
+                        // upper half of the S columns: the upper 64 keys first (their S
+                        // columns are already in registers), then the lower 64 keys,
+                        // reloaded (their P columns overwrite S columns 64..95, consumed).
+                        // (the element-wise mask exists only in the masked instantiation,
+                        // chosen once per tile)
                         if (masked)
-                            exp_half<BF16, true>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                            exp_half<BF16, true>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
                         else
-                            exp_half<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                            exp_half<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                        {
+                            uint32_t lo[64];
+                            tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                            tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
+                            tmem_wait_ld();
+                            if constexpr (C::SEP) {
+                                // last read of this S: the MMA warp may overwrite it now
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
+                            }
+                            if (masked)
+                                exp_half<BF16, true>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                            else
+                                exp_half<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                        }
                     }
 
                 }

@@ -262,9 +262,10 @@ def time_e2e(af, w, dev, steps, warmup):
 
 # ----------------------------------------------------------------- oracle (CPU)
 
-def oracle_sample(w, n_heads: int):
+def oracle_sample(w, n_heads: int, reps: int = 1):
     """Time the CPU fp64 oracle on the first n_heads (b, h) heads of workload
-    w (all rows of each); returns (seconds, flops of the sample, threads)."""
+    w (all rows of each), reps times over; returns (seconds, flops of the
+    sample, threads)."""
     import oracle
     q, k, v = make_workload_inputs(w)
     BH = w.B * w.H
@@ -273,25 +274,34 @@ def oracle_sample(w, n_heads: int):
     threads = os.cpu_count() or 1
     oracle.load()
     t0 = time.perf_counter()
-    oracle.attention(qf, kf, vf, w.mask, w.block_size, w.sm_scale, nthreads=threads)
+    for _ in range(reps):
+        oracle.attention(qf, kf, vf, w.mask, w.block_size, w.sm_scale, nthreads=threads)
     dt = time.perf_counter() - t0
     import attention_forward_15_gb300 as af
     flops, _ = af.work(1, n_heads, w.L, w.D, w.mask, w.block_size, w.dtype)
-    return dt, flops, threads
+    return dt, flops * reps, threads
 
 
 def cpu_baseline(w, target_s: float = 10.0):
     """Oracle throughput on the host cores on a bounded sample of workload w
-    (calibrated on one head, then enough heads for about target_s seconds)."""
+    (calibrated on one head, then enough heads for about target_s seconds; a
+    workload whose every head takes less than that is run whole, repeated)."""
     dt1, f1, threads = oracle_sample(w, 1)
     n = max(1, min(w.B * w.H, int(target_s / max(dt1, 1e-3))))
+    reps = 1
     if n > 1:
         dt, f, threads = oracle_sample(w, n)
     else:
         dt, f = dt1, f1
+    if n == w.B * w.H and dt < 0.5 * target_s:
+        reps = max(1, min(64, int(target_s / max(dt, 1e-3))))
+        if reps > 1:
+            dt, f, threads = oracle_sample(w, n, reps)
+    what = f"all {w.L} rows of {n} of the {w.B * w.H} (b,h) heads"
+    if reps > 1:
+        what += f", the whole workload {reps} times"
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"all {w.L} rows of {n} of the {w.B * w.H} (b,h) heads, fp64, "
-                      f"{dt:.2f} s wall"}
+            "sample": f"{what}, fp64, {dt:.2f} s wall"}
 
 
 # ----------------------------------------------------------------- ranks
