@@ -712,18 +712,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     const uint32_t vpos = rc + 1;
                     rc += 2;                                            // K and V entries
                     const uint32_t vslot = vpos % C::RING;
-                    bool v_ready = false;
+                    // V lands long before the first P of the tile: wait for it first,
+                    // so that only the P-ready wait stands between P and its MMAs
+                    ok = wait_warp(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u, kSiteKvFullV);
+                    if (!ok) break;
 #pragma unroll
                     for (int w = 0; w < 2; ++w) {
                         if (!ok || !(w == 0 ? use0 : use1)) continue;
                         ok = wait_warp(bar(C::B_PFULL + w), pn[w] & 1u, kSitePFull);
                         if (!ok) break;
                         ++pn[w];
-                        if (!v_ready) {
-                            ok = wait_warp(bar(C::B_KVFULL + vslot), (vpos / C::RING) & 1u, kSiteKvFullV);
-                            if (!ok) break;
-                            v_ready = true;
-                        }
                         tc_fence_after();
                         issue_pv(w, w, vslot, npv[w] > 0);
                         ++npv[w];
