@@ -350,7 +350,23 @@ __device__ __forceinline__ void exp_chunk(const uint32_t *v, int base, int rel_l
     tmem_st16(dst, pk);
 }
 
-// ---------------------------------------------------------------- kernel
+// exp_chunk without the mask and without the store: the 16 packed pairs stay
+// in `pk` for the caller to store later.
+template <bool BF16>
+__device__ __forceinline__ void exp_pack(const uint32_t *v, float sc, float neg_m, float2 (&acc)[4],
+                                         uint32_t (&pk)[16]) {
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                    sc2, nm2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
+        pk[e] = pack2<BF16>(pp.x, pp.y);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int D, bool BF16, bool PAIR>
@@ -868,18 +884,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             bool fits = m_ref != -INFINITY &&
                                         row_extreme64(sv, sc >= 0.f) * sc <= lim;
                             if (__all_sync(0xffffffffu, fits)) {
-                                // P and O of this lane are still read/written by the
-                                // previous tile's P.V until it completes.
-                                ok = wait_pv(wg);
-                                if (!ok) break;
-                                tc_fence_after();
                                 neg_m = -m_ref;
-                                // keys 0..63 from registers while keys 64..127 load
-                                exp_chunk<BF16, false>(sv, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                                // keys 0..63 from registers while keys 64..127 load; their
+                                // P waits in registers while the previous tile's P.V still
+                                // reads the P columns
+                                uint32_t pk0[16], pk1[16];
+                                exp_pack<BF16>(sv, sc, neg_m, acc, pk0);
                                 tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-                                exp_chunk<BF16, false>(sv + 32, 32, rel_lo, rel_hi, sc, neg_m, acc,
-                                                       p_addr + 16);
+                                exp_pack<BF16>(sv + 32, sc, neg_m, acc, pk1);
                                 tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                                ok = wait_pv(wg);
+                                if (!ok) {
+                                    tmem_wait_ld();
+                                    break;
+                                }
+                                tc_fence_after();
+                                tmem_st16(p_addr, pk0);
+                                tmem_st16(p_addr + 16, pk1);
                                 tmem_wait_ld();
                                 fits = row_extreme64(sv, sc >= 0.f) * sc <= lim;
                                 if (__all_sync(0xffffffffu, fits)) {
