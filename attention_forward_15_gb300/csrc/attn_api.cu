@@ -157,7 +157,23 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
     if (rc == ATTN_OK) rc = encode_map(&tv, v, prm.BH, prm.L, D, dtype);
     if (rc != ATTN_OK) return rc;
     const int grid = prm.n_units < st.sms ? prm.n_units : st.sms;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+    // Programmatic dependent launch: the CTAs may be scheduled while the
+    // previous kernel of the stream finishes; the kernel waits for that
+    // kernel's completion (griddepcontrol.wait) before its first global access.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -420,6 +420,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Launched as a programmatic dependent: everything above touches only this
+    // CTA's own resources; global memory may be written by the previous kernel
+    // of the stream until it completes.  Dependents of this kernel may be
+    // scheduled from now on (they wait for its completion in the same way).
+    griddep_wait();
+    griddep_launch_dependents();
     // Allocating all 512 columns can only start at lane 0, column 0, so the TMEM
     // base is the constant 0 (which keeps every TMEM address a compile-time
     // offset).  Anything else is reported and no work is done.

@@ -75,7 +75,10 @@ typedef enum {
  *   stream      a cudaStream_t (NULL = the legacy default stream).
  *
  * Returns ATTN_OK once the kernel is enqueued; the outputs are valid after
- * the stream is synchronised.  Argument errors are detected on the host
+ * the stream is synchronised.  The kernel is launched as a programmatic
+ * dependent of the previous kernel on `stream` (its CTAs may be scheduled
+ * while that kernel finishes, but they wait for its completion before any
+ * global memory access), so stream ordering is unchanged for the caller.  Argument errors are detected on the host
  * before any CUDA call and nothing is launched or written.  A failed launch
  * returns ATTN_ERR_CUDA.  Every wait inside the kernel is bounded (about one
  * second); if one runs out the kernel stops, frees its tensor memory and
