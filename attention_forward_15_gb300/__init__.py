@@ -17,6 +17,8 @@ from . import _build_ext
 
 DENSE, CAUSAL, BLOCK_DIAG = 0, 1, 2
 F16, BF16 = 0, 1
+# head dims with a kernel of their own; any multiple of 8 up to 256 is accepted
+# (it runs in the next one up, the extra columns loaded as zeros)
 HEAD_DIMS = (64, 128, 256)
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_BLOCK_SIZE",

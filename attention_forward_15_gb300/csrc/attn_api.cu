@@ -31,7 +31,13 @@ DeviceState g_dev[kMaxDevices];
 int g_inject = 0;   // fault-injection mode for the next attn_fwd calls (tests only)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-int head_dim_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : (D == 256 ? 2 : -1)); }
+// Head dims: any multiple of 8 from 8 to 256.  Kernels exist for 64, 128 and
+// 256; a smaller head dim runs in the next one up, its tensor maps declaring
+// the true width so that the missing columns load as zeros (they add nothing to
+// Q K^T and give zero columns of O, which are not stored).
+bool head_dim_ok(int D) { return D >= 8 && D <= 256 && D % 8 == 0; }
+int kernel_dim(int D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
+int head_dim_index(int D) { return kernel_dim(D) == 64 ? 0 : (kernel_dim(D) == 128 ? 1 : 2); }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -40,7 +46,7 @@ int validate_shape(int B, int H, int L, int D, int mask_kind, int block_size, in
     if (B < 0 || H < 0 || L < 0) return ATTN_ERR_SHAPE;
     if (mask_kind < ATTN_MASK_DENSE || mask_kind > ATTN_MASK_BLOCK_DIAG) return ATTN_ERR_UNSUPPORTED;
     if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-    if (head_dim_index(D) < 0) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(D)) return ATTN_ERR_UNSUPPORTED;
     if (mask_kind == ATTN_MASK_BLOCK_DIAG) {
         if (block_size <= 0) return ATTN_ERR_BLOCK_SIZE;
         if (L > 0 && L % block_size != 0) return ATTN_ERR_BLOCK_SIZE;
@@ -61,7 +67,7 @@ struct Plan {
 
 Plan make_plan(int B, int H, int L, int D) {
     Plan pl;
-    pl.pair = D <= 128;
+    pl.pair = kernel_dim(D) <= 128;
     pl.n_qt = (L + attn::BM - 1) / attn::BM;
     pl.n_kv = (L + attn::BN - 1) / attn::BN;
     const int per_bh = pl.pair ? (pl.n_qt + 1) / 2 : pl.n_qt;
@@ -75,10 +81,16 @@ bool kv_fits_l2(int BH, int L, int D) {
     return 2.0 * BH * static_cast<double>(L) * D * 2.0 <= 64.0 * 1024 * 1024;
 }
 
-int threads_for(int D) { return D <= 128 ? Cfg<64, true>::THREADS : Cfg<256, false>::THREADS; }
+int threads_for(int D) {
+    switch (kernel_dim(D)) {
+        case 64: return Cfg<64, true>::THREADS;
+        case 128: return Cfg<128, true>::THREADS;
+        default: return Cfg<256, false>::THREADS;
+    }
+}
 
 int smem_for(int D) {
-    switch (D) {
+    switch (kernel_dim(D)) {
         case 64: return Cfg<64, true>::SMEM_BYTES;
         case 128: return Cfg<128, true>::SMEM_BYTES;
         default: return Cfg<256, false>::SMEM_BYTES;
@@ -152,9 +164,9 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
         }
     }
     CUtensorMap tq, tk, tv;
-    int rc = encode_map(&tq, q, prm.BH, prm.L, D, dtype);
-    if (rc == ATTN_OK) rc = encode_map(&tk, k, prm.BH, prm.L, D, dtype);
-    if (rc == ATTN_OK) rc = encode_map(&tv, v, prm.BH, prm.L, D, dtype);
+    int rc = encode_map(&tq, q, prm.BH, prm.L, prm.d_out, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tk, k, prm.BH, prm.L, prm.d_out, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tv, v, prm.BH, prm.L, prm.d_out, dtype);
     if (rc != ATTN_OK) return rc;
     const int grid = prm.n_units < st.sms ? prm.n_units : st.sms;
     // Programmatic dependent launch: the CTAs may be scheduled while the
@@ -270,10 +282,11 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
     prm.inject = g_inject;
     prm.kv_keep = kv_fits_l2(prm.BH, L, D) ? 1 : 0;
+    prm.d_out = D;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == ATTN_BF16;
-    switch (D) {
+    switch (kernel_dim(D)) {
         case 64:
             return bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
                         : launch<64, false, true>(*st, q, k, v, prm, dtype, s);
@@ -399,9 +412,10 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, voi
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
     prm.inject = 0;
     prm.kv_keep = kv_fits_l2(prm.BH, L, D) ? 1 : 0;
+    prm.d_out = D;
 
     const bool bf16 = dtype == ATTN_BF16;
-    switch (D) {
+    switch (kernel_dim(D)) {
         case 64:
             rc = bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
                       : launch<64, false, true>(*st, q, k, v, prm, dtype, s);

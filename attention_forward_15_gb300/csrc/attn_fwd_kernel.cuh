@@ -70,6 +70,8 @@ struct FwdParams {
     int kv_keep;             // 1: K/V loads ask L2 to keep them (all K/V fit in L2)
     int inject;              // test hook: 1 = the producer issues no copies, so every
                              // consumer's bounded wait runs out (0 in normal use)
+    int d_out;               // head dim of Q, K, V and O in memory (<= D of the kernel;
+                             // the columns past it load as zeros and are not stored)
 };
 
 template <int D, bool PAIR>
@@ -1039,9 +1041,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const float inv_l = 1.f / l;
             const uint32_t o_addr = tmem + lane_off + C::o_col(PAIR ? wg : 0);
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
-                                                   ((static_cast<size_t>(U.bh) * p.L + i) * D) * 2);
+                                                   ((static_cast<size_t>(U.bh) * p.L + i) * p.d_out) * 2);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 32 && 32 * c < p.d_out; ++c) {
                 uint32_t raw[32];
                 tmem_ld32(o_addr + 32 * c, raw);
                 tmem_wait_ld();
@@ -1053,8 +1055,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (row_valid) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
-                        dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
-                                                     w16[4 * v4 + 3]);
+                        if (32 * c + 8 * v4 < p.d_out)
+                            dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
+                                                         w16[4 * v4 + 3]);
                 }
             }
             if (row_valid && p.lse != nullptr) {

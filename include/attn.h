@@ -66,7 +66,10 @@ typedef enum {
  *   lse         output, [B, H, L] fp32, device memory; may be NULL (not written).
  *   B, H, L     batch, heads, sequence length (queries = keys = L).  A zero
  *               size is an empty problem: ATTN_OK, nothing is launched.
- *   D           head dim: 64, 128 or 256.
+ *   D           head dim: a multiple of 8 from 8 to 256.  Kernels exist for
+ *               64, 128 and 256; any other D runs in the next one up, the
+ *               columns past D loading as zeros (same results, the MMA work of
+ *               the larger head dim).
  *   mask_kind   an attn_mask_kind.
  *   block_size  the block size bs of ATTN_MASK_BLOCK_DIAG (ignored otherwise);
  *               bs must divide L and be a divisor or a multiple of 128.

@@ -53,8 +53,10 @@ def _fwd(lib, B=1, H=1, L=256, D=128, mask=0, bs=0, scale=0.1, dtype=0, ptrs=(16
 
 def test_host_validation_before_any_cuda_call(lib):
     # every case is rejected on the host: no device is touched
-    assert _fwd(lib, D=96) == 4
-    assert _fwd(lib, D=32) == 4
+    assert _fwd(lib, D=100) == 4                  # head dims are multiples of 8 ...
+    assert _fwd(lib, D=4) == 4
+    assert _fwd(lib, D=264) == 4                  # ... from 8 to 256
+    assert _fwd(lib, D=0) == 4
     assert _fwd(lib, dtype=2) == 4
     assert _fwd(lib, mask=3) == 4
     assert _fwd(lib, B=-1) == 2

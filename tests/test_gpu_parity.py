@@ -113,6 +113,40 @@ def test_small_all_elements(af, case):
     _full_case(af, *case)
 
 
+# Head dims other than 64, 128 and 256 run in the next kernel up with the
+# missing columns loaded as zeros; these cover each kernel size from below.
+OTHER_DIMS = [
+    # (B, H, L, D, mask, bs, dtype)
+    (1, 2, 256, 8, DENSE, 0, torch.float16),
+    (2, 2, 256, 16, DENSE, 0, torch.float16),
+    (1, 2, 200, 16, CAUSAL, 0, torch.bfloat16),
+    (1, 3, 384, 32, DENSE, 0, torch.bfloat16),
+    (1, 2, 333, 32, CAUSAL, 0, torch.float16),
+    (1, 2, 512, 48, BLOCK_DIAG, 64, torch.float16),
+    (1, 2, 384, 96, CAUSAL, 0, torch.bfloat16),
+    (1, 2, 300, 112, DENSE, 0, torch.float16),
+    (1, 2, 256, 160, DENSE, 0, torch.bfloat16),
+    (1, 2, 384, 192, CAUSAL, 0, torch.float16),
+    (1, 2, 512, 200, BLOCK_DIAG, 128, torch.bfloat16),
+    (1, 1, 200, 248, DENSE, 0, torch.float16),
+]
+
+
+@pytest.mark.parametrize("case", OTHER_DIMS, ids=lambda c: "B{}H{}L{}D{}m{}bs{}{}".format(
+    *c[:6], "f16" if c[6] == torch.float16 else "bf16"))
+def test_other_head_dims_all_elements(af, case):
+    _full_case(af, *case)
+
+
+@pytest.mark.parametrize("D", [16, 32])
+@pytest.mark.parametrize("causal", [False, True])
+def test_page_small_head_dims(af, D, causal):
+    """Head dims 16 and 32, which the Fused Attention page's kernel accepts,
+    with the page's input recipe (seed 20, N(0, 0.5), sm_scale 0.5)."""
+    _full_case(af, 2, 4, 1024, D, CAUSAL if causal else DENSE, 0, torch.float16, scale=0.5, seed=20,
+               std=0.5, guard=False)
+
+
 @pytest.mark.parametrize("mask,bs", [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 64)])
 def test_large_scores_exercise_rescaling(af, mask, bs):
     """N(0, 3^2) inputs: scaled scores have a standard deviation near 9, so the
@@ -159,10 +193,10 @@ def test_empty_and_no_lse(af):
 
 def test_argument_errors(af):
     dev = torch.device("cuda", 0)
-    q = torch.zeros((1, 1, 256, 96), dtype=torch.float16, device=dev)
+    q = torch.zeros((1, 1, 256, 100), dtype=torch.float16, device=dev)
     with pytest.raises(af.AttnError) as e:
         af.fwd(q, q, q)
-    assert e.value.status == 4                      # head dim 96 unsupported
+    assert e.value.status == 4                      # head dim 100: not a multiple of 8
     q = torch.zeros((1, 1, 256, 64), dtype=torch.float16, device=dev)
     with pytest.raises(af.AttnError) as e:
         af.fwd(q, q, q, BLOCK_DIAG, 48)

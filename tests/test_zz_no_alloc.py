@@ -66,8 +66,9 @@ def test_noalloc_matches_regular_entry_point(lib, case):
 
 
 def test_noalloc_rejects_bad_arguments(lib):
-    rc = lib.attn_fwd_noalloc(16, 16, 16, 16, None, 1, 1, 256, 96, DENSE, 0, 0.1, 0, None, None)
-    assert rc == 4
+    # placeholder pointers: every call here must be rejected on the host
+    rc = lib.attn_fwd_noalloc(16, 16, 16, 16, None, 1, 1, 256, 100, DENSE, 0, 0.1, 0, None, None)
+    assert rc == 4                                    # head dim not a multiple of 8
     rc = lib.attn_fwd_noalloc(16, 16, 16, 16, None, 1, 1, 256, 64, BLOCK_DIAG, 48, 0.1, 0,
                               None, None)
     assert rc == 3
