@@ -503,12 +503,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     qpar ^= 1u << q;
                     qused |= 1u << q;
                 }
-                for (int j = U.ulo; j < U.uhi && ok; ++j) {
-                    if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
+                // one K or V tile of key tile j as EPT ring entries
+                auto load_kv = [&](int kind, int j) {
 #pragma unroll
-                    for (int ke = 0; ke < 2 * C::EPT; ++ke) {   // K entries, then V entries
+                    for (int e = 0; e < C::EPT; ++e) {
                         if (!ok) continue;
-                        const int kind = ke / C::EPT, e = ke % C::EPT;
                         const uint32_t slot = rc % C::RING;
                         ok = wait_warp(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u,
                                        kSiteKvEmpty);
@@ -526,6 +525,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                             j * BN, U.bh, bar(C::B_KVFULL + slot));
                         }
                         ++rc;
+                    }
+                };
+                if constexpr (PAIR) {
+                    // per key tile: K, then V
+                    for (int j = U.ulo; j < U.uhi && ok; ++j) {
+                        if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
+                        load_kv(0, j);
+                        load_kv(1, j);
+                    }
+                } else {
+                    // K runs one tile ahead of V: K(0), then K(t+1), V(t) for each t, so
+                    // the next S never waits for the ring space of the V in use
+                    const int n = U.hi[0] - U.lo[0];
+                    if (n > 0) load_kv(0, U.lo[0]);
+                    for (int t = 0; t < n && ok; ++t) {
+                        if (t + 1 < n) load_kv(0, U.lo[0] + t + 1);
+                        load_kv(1, U.lo[0] + t);
                     }
                 }
             }
@@ -650,8 +666,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     const int n = U.hi[0] - U.lo[0];
                     const uint32_t base = rc;
                     rc += 2u * C::EPT * static_cast<uint32_t>(n);
+                    // ring positions in the order the copies are issued: K(0), then
+                    // K(t+1), V(t) for each t
+                    auto pos_k = [&](int t) -> uint32_t {
+                        return base + static_cast<uint32_t>(C::EPT * (t == 0 ? 0 : 2 * t - 1));
+                    };
+                    auto pos_v = [&](int t) -> uint32_t {
+                        return base + static_cast<uint32_t>(C::EPT * (t + 1 < n ? 2 * t + 2 : 2 * t + 1));
+                    };
                     auto do_s = [&](int t) -> bool {
-                        const uint32_t kpos = base + 2u * C::EPT * t;
+                        const uint32_t kpos = pos_k(t);
                         const uint64_t qd = sdesc_sw128(q_smem + qb * C::NQ * C::TILE_BYTES, 16, 1024);
                         const uint32_t d_tmem = tmem + C::s_col(t & 1);
 #pragma unroll
@@ -669,11 +693,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                 const uint64_t koff = (kl >> 2) * (C::CHUNK_BYTES >> 4) + (kl & 3) * 2;
                                 mma_ss(d_tmem, qd + qoff, kd + koff, IDESC_S, kk > 0 ? 1u : 0u);
                             }
+                            // this K entry is free once its k-steps are done
+                            mma_commit(bar(C::B_KVEMPTY + kslot));
                         }
                         mma_commit(bar(C::B_SFULL + (t & 1)));
-#pragma unroll
-                        for (int e = 0; e < C::EPT; ++e)
-                            mma_commit(bar(C::B_KVEMPTY + (kpos + e) % C::RING));
                         if (t == n - 1) mma_commit(bar(C::B_QEMPTY + qb * C::NQ));
                         return true;
                     };
@@ -685,7 +708,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         ok = wait_warp(bar(C::B_PFULL + b), pn[b] & 1u, kSitePFull);
                         if (!ok) break;
                         ++pn[b];
-                        const uint32_t vpos = base + 2u * C::EPT * t + C::EPT;
+                        const uint32_t vpos = pos_v(t);
 #pragma unroll
                         for (int e = 0; e < C::EPT; ++e) {
                             if (!ok) continue;
@@ -702,12 +725,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             for (int kk = 0; kk < BN / 16; ++kk)
                                 mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128),
                                        IDESC_PVE, (t > 0 || kk > 0) ? 1u : 0u);
+                            // this V entry is free once its part of P.V is done
+                            mma_commit(bar(C::B_KVEMPTY + vslot));
                         }
                         if (!ok) break;
                         mma_commit(bar(C::B_ODONE + b));
-#pragma unroll
-                        for (int e = 0; e < C::EPT; ++e)
-                            mma_commit(bar(C::B_KVEMPTY + (vpos + e) % C::RING));
                     }
                 }
             }
