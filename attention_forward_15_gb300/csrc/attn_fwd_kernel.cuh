@@ -297,6 +297,25 @@ __device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool wan
     return fminf(fmin3(a[0], a[1], a[2]), a[3]);
 }
 
+// max (or min) of 32 raw scores, two chains.
+__device__ __forceinline__ float row_extreme32(const uint32_t *v, bool want_max) {
+    float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
+    if (want_max) {
+#pragma unroll
+        for (int c = 2; c < 32; c += 4) {
+            a = fmax3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            b = fmax3(b, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        }
+        return fmaxf(a, b);
+    }
+#pragma unroll
+    for (int c = 2; c < 32; c += 4) {
+        a = fmin3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+        b = fmin3(b, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    }
+    return fminf(a, b);
+}
+
 // p = exp2(s * sc - m) for a 64-key half (keys base..base+63 of the tile):
 // packed fma, MUFU ex2, packed partial sums into acc[8], rounding to 16-bit
 // pairs and one 32-column TMEM store at `dst`.  The packed fp32x2 builtins
@@ -899,6 +918,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     }
                 } else {
                     bool done = false;
+                    if constexpr (PAIR && !C::SEP) {
+                        // One pass against the running reference max with P over the
+                        // upper half of S: the whole row is checked against the
+                        // reference before the first P store, so a tile that climbs more
+                        // than the rescale threshold above it falls to the two-pass path
+                        // below with S intact.  Keys 64..127 stay in registers (their
+                        // columns take P); keys 0..63 are read twice.
+                        if (t > 0 && !masked) {
+                            uint32_t hi[64], lo[32];
+                            tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                            tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
+                            tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                            tmem_wait_ld();
+                            const bool want_max = sc >= 0.f;
+                            float ext = row_extreme64(hi, want_max);
+                            const float e0 = row_extreme32(lo, want_max);
+                            ext = want_max ? fmaxf(ext, e0) : fminf(ext, e0);
+                            tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                            tmem_wait_ld();
+                            const float e1 = row_extreme32(lo, want_max);
+                            ext = want_max ? fmaxf(ext, e1) : fminf(ext, e1);
+                            const bool fits = m_ref != -INFINITY && ext * sc <= m_ref + kRescaleLog2;
+                            if (__all_sync(0xffffffffu, fits)) {
+                                neg_m = -m_ref;
+                                tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
+                                exp_chunk<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                                exp_chunk<BF16, false>(hi + 32, 96, rel_lo, rel_hi, sc, neg_m, acc,
+                                                       p_addr + 48);
+                                tmem_wait_ld();
+                                tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                                exp_chunk<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                                tmem_wait_ld();
+                                exp_chunk<BF16, false>(hi, 32, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 16);
+                                done = true;
+                            }
+                        }
+                    }
                     if constexpr (C::SEP) {
                         // One pass against the running reference max.  S stays in TMEM
                         // until this tile's S-free arrival (P has columns of its own),
