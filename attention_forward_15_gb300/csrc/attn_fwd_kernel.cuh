@@ -978,13 +978,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                 exp_pack<BF16>(sv, sc, neg_m, acc, pk0);
                                 tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
                                 exp_pack<BF16>(sv + 32, sc, neg_m, acc, pk1);
-                                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                                // No TMEM load is left in flight across the wait below: its
+                                // slow path is a call, around which live registers may be
+                                // saved and restored, and the destination registers of a
+                                // load are undefined until tcgen05.wait::ld.
+                                tmem_wait_ld();
                                 ok = wait_pv(wg);
-                                if (!ok) {
-                                    tmem_wait_ld();
-                                    break;
-                                }
+                                if (!ok) break;
                                 tc_fence_after();
+                                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
                                 tmem_st16(p_addr, pk0);
                                 tmem_st16(p_addr + 16, pk1);
                                 tmem_wait_ld();
