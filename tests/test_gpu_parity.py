@@ -234,6 +234,57 @@ FULL = ["blockdiag_b1h2n256d128_bs64_f16", "dense_b4h16l1024d64_f16", "causal_b2
         "causal_b1h32l32768d128_bf16", "dense_b1h16l16384d256_bf16"]
 
 
+@pytest.mark.parametrize("name", ["dense_b4h16l1024d64_f16", "causal_b2h32l4096d128_bf16"])
+def test_full_size_every_element(af, name):
+    """The benchmark's headline workload and the causal workload at full size,
+    every element of O and lse against the oracle (a few seconds of CPU)."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    dev = torch.device("cuda", 0)
+    o, lse = af.fwd(q.to(dev), k.to(dev), v.to(dev), w.mask, w.block_size, w.sm_scale)
+    torch.cuda.synchronize()
+    O_ref, lse_ref = oracle.attention(q, k, v, w.mask, w.block_size, w.sm_scale)
+    _check(o.cpu(), lse.cpu(), O_ref, lse_ref, w.dtype, name)
+
+
+def _attended_keys(mask, bs, L, i):
+    if mask == DENSE:
+        return 0, L
+    if mask == CAUSAL:
+        return 0, i + 1
+    return (i // bs) * bs, (i // bs) * bs + bs
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_properties(af, name):
+    """Properties that hold at any size, on rows spread over every head: each O
+    row lies inside the range of the attended V rows (column by column, up to
+    the output rounding), and lse is at least the largest attended scaled score
+    and at most that plus ln(number of attended keys)."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    dev = torch.device("cuda", 0)
+    o, lse = af.fwd(q.to(dev), k.to(dev), v.to(dev), w.mask, w.block_size, w.sm_scale)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(7)
+    BH = w.B * w.H
+    qf, kf, vf = (t.reshape(BH, w.L, w.D) for t in (q, k, v))
+    of, lf = o.cpu().reshape(BH, w.L, w.D), lse.cpu().reshape(BH, w.L)
+    slack = 2e-3 if w.dtype == torch.float16 else 1e-2
+    for bh in range(BH):
+        for i in g.integers(0, w.L, size=2):
+            i = int(i)
+            lo, hi = _attended_keys(w.mask, w.block_size, w.L, i)
+            vs = vf[bh, lo:hi].double()
+            orow = of[bh, i].double()
+            assert (orow >= vs.min(0).values - slack).all(), f"{name} bh{bh} row {i}: O below V range"
+            assert (orow <= vs.max(0).values + slack).all(), f"{name} bh{bh} row {i}: O above V range"
+            s = (kf[bh, lo:hi].double() @ qf[bh, i].double()) * w.sm_scale
+            smax = float(s.max())
+            assert smax - 1e-3 <= float(lf[bh, i]) <= smax + math.log(hi - lo) + 1e-3, \
+                f"{name} bh{bh} row {i}: lse {float(lf[bh, i])} outside [{smax}, {smax + math.log(hi - lo)}]"
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workloads_sampled(af, name):
     w = WORKLOADS[name]
