@@ -37,6 +37,8 @@ _SIGNATURES = {
                                                ctypes.POINTER(ctypes.c_uint)]),
     "attn_fwd_plan": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_int)] * 4),
     "attn_abi_version": (ctypes.c_int, []),
+    "attn_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_int] * 6 +
+                      [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
 }
 
 _lib = None
@@ -161,29 +163,40 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int = DENS
 
 def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int = DENSE,
              block_size: int = 0, sm_scale: float | None = None, device: int = 0,
-             staging: dict | None = None):
-    """Forward of HOST tensors: copies q, k, v to the GPU, runs ``fwd`` and
-    copies o and lse back into host tensors (pinned when ``staging`` holds
-    them).  ``staging`` may hold preallocated device buffers ``q_d, k_d, v_d,
-    o_d, lse_d`` and host outputs ``o_h, lse_h`` to reuse across calls.
-    Returns ``(o_host, lse_host)`` after synchronising the stream."""
+             staging: dict | None = None, return_lse: bool = True):
+    """Forward of HOST tensors through ``attn_fwd_host``: the library copies q,
+    k, v to the GPU, runs the forward on the current stream of ``device``,
+    copies o and lse back and synchronises.  ``staging`` keeps the device
+    buffers (``q_d, k_d, v_d, o_d, lse_d``) and the page-locked host outputs
+    (``o_h, lse_h``) for reuse across calls.  Returns ``(o_host, lse_host)``."""
+    lib = load_library()
     st = staging if staging is not None else {}
     dev = torch.device("cuda", device)
-    names = ("q_d", "k_d", "v_d")
-    for name, t in zip(names, (q, k, v)):
+    for t in (q, k, v):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("fwd_host takes contiguous host tensors")
+    B, H, L, D = (int(x) for x in q.shape)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    for name in ("q_d", "k_d", "v_d", "o_d"):
         if name not in st:
-            st[name] = torch.empty(t.shape, dtype=t.dtype, device=dev)
-        st[name].copy_(t, non_blocking=True)
-    o_d, lse_d = fwd(st["q_d"], st["k_d"], st["v_d"], mask_kind, block_size, sm_scale,
-                     out=st.get("o_d"), lse_out=st.get("lse_d"))
-    st["o_d"], st["lse_d"] = o_d, lse_d
+            st[name] = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    if "lse_d" not in st:
+        st["lse_d"] = torch.empty((B, H, L), dtype=torch.float32, device=dev)
     if "o_h" not in st:
-        st["o_h"] = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
-        st["lse_h"] = torch.empty(lse_d.shape, dtype=lse_d.dtype, pin_memory=True)
-    st["o_h"].copy_(o_d, non_blocking=True)
-    st["lse_h"].copy_(lse_d, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
-    return st["o_h"], st["lse_h"]
+        st["o_h"] = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        st["lse_h"] = torch.empty((B, H, L), dtype=torch.float32, pin_memory=True)
+    with torch.cuda.device(dev):
+        s = torch.cuda.current_stream(dev)
+        rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), st["o_h"].data_ptr(),
+                               st["lse_h"].data_ptr() if return_lse else None,
+                               st["q_d"].data_ptr(), st["k_d"].data_ptr(), st["v_d"].data_ptr(),
+                               st["o_d"].data_ptr(), st["lse_d"].data_ptr(), B, H, L, D,
+                               int(mask_kind), int(block_size), float(sm_scale),
+                               _dtype_code(q.dtype), ctypes.c_void_p(s.cuda_stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd_host")
+    return st["o_h"], (st["lse_h"] if return_lse else None)
 
 
 def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,

@@ -150,6 +150,32 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
                      int B, int H, int L, int D, int mask_kind, int block_size,
                      float sm_scale, int dtype, void *stream, unsigned int *status_out);
 
+/*
+ * attn_fwd_host -- the whole forward for inputs and outputs in HOST memory:
+ * copies q, k, v to the device, runs attn_fwd, copies o (and lse) back and
+ * synchronises `stream` before returning, so the host outputs are valid on
+ * return.
+ *
+ *   q_h, k_h, v_h   host inputs, [B, H, L, D] of `dtype` (page-locked memory
+ *                   keeps the copies asynchronous and at full speed).
+ *   o_h             host output, [B, H, L, D] of `dtype`.
+ *   lse_h           host output, [B, H, L] fp32; may be NULL.
+ *   q_d, k_d, v_d, o_d, lse_d
+ *                   device buffers of the same shapes that the caller owns and
+ *                   may reuse across calls (lse_d may be NULL when lse_h is).
+ *   the rest        as for attn_fwd.
+ *
+ * One cudaMemcpyAsync per tensor, then the kernel, on `stream`.  Returns an
+ * attn_status: argument errors as attn_fwd (plus ATTN_ERR_NULL for a missing
+ * host or device buffer) before any copy; ATTN_ERR_CUDA if a copy, the launch
+ * or the synchronisation fails.  A device-side timeout is read with
+ * attn_last_device_status, as for attn_fwd.
+ */
+int attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                  void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
+                  int B, int H, int L, int D, int mask_kind, int block_size,
+                  float sm_scale, int dtype, void *stream);
+
 /* Number of work units and CTAs attn_fwd would launch for these arguments on
  * the current device (for tests and reports); returns an attn_status. */
 int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size,

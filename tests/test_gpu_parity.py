@@ -191,6 +191,30 @@ def test_empty_and_no_lse(af):
     assert np.abs(o.double().cpu().numpy() - O_ref).max() <= TOL_O[torch.float16]
 
 
+@pytest.mark.parametrize("mask,bs,dt", [(DENSE, 0, torch.float16), (CAUSAL, 0, torch.bfloat16),
+                                         (BLOCK_DIAG, 64, torch.float16)])
+def test_host_buffer_entry_point(af, mask, bs, dt):
+    """attn_fwd_host (host inputs and outputs, copies inside the call) gives the
+    same bytes as attn_fwd on device buffers, call after call with reused
+    staging buffers, and matches the oracle."""
+    q, k, v = (t.pin_memory() for t in make_qkv(2, 3, 640, 64, dt, seed=5))
+    dev = torch.device("cuda", 0)
+    o_ref, lse_ref = af.fwd(q.to(dev), k.to(dev), v.to(dev), mask, bs, 0.125)
+    torch.cuda.synchronize()
+    staging = {}
+    for _ in range(2):
+        o_h, lse_h = af.fwd_host(q, k, v, mask, bs, 0.125, staging=staging)
+        assert torch.equal(o_h, o_ref.cpu()) and torch.equal(lse_h, lse_ref.cpu())
+    O, L = oracle.attention(q, k, v, mask, bs, 0.125)
+    _check(o_h, lse_h, O, L, dt, "fwd_host")
+    o2, l2 = af.fwd_host(q, k, v, mask, bs, 0.125, return_lse=False)
+    assert l2 is None and torch.equal(o2, o_ref.cpu())
+    with pytest.raises(af.AttnError) as e:                  # head dim 44: not a multiple of 8
+        af.fwd_host(q[..., :44].contiguous(), k[..., :44].contiguous(), v[..., :44].contiguous(),
+                    mask, bs, 0.125)
+    assert e.value.status == 4
+
+
 def test_argument_errors(af):
     dev = torch.device("cuda", 0)
     q = torch.zeros((1, 1, 256, 100), dtype=torch.float16, device=dev)
