@@ -74,6 +74,17 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.attn_oracle_widen.restype = ctypes.c_double
         lib.attn_oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
+        lib.attn_oracle_widen_e5m2.restype = ctypes.c_double
+        lib.attn_oracle_widen_e5m2.argtypes = [ctypes.c_uint8]
+        lib.attn_oracle_round_e5m2.restype = ctypes.c_double
+        lib.attn_oracle_round_e5m2.argtypes = [ctypes.c_double]
+        lib.attn_oracle_fp8v.restype = ctypes.c_int
+        lib.attn_oracle_fp8v.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            ctypes.c_int, ctypes.c_long, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_long,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         _libs[mutant] = lib
         return lib
 
@@ -134,3 +145,51 @@ def attention(q, k, v, mask_kind: int, block_size: int = 0, sm_scale: float | No
         raise ValueError(f"oracle rejected arguments (B={B} H={H} L={L} D={D} "
                          f"mask={mask_kind} bs={block_size})")
     return O, lse
+
+
+def widen_e5m2(byte: int, mutant: int = 0) -> float:
+    return load(mutant).attn_oracle_widen_e5m2(byte)
+
+
+def round_e5m2(x: float, mutant: int = 0) -> float:
+    return load(mutant).attn_oracle_round_e5m2(float(x))
+
+
+def attention_fp8v(q, k, vt, mask_kind: int, block_size: int = 0, sm_scale: float | None = None,
+                   rows=None, nthreads: int = 0, mutant: int = 0):
+    """The FP8 P.V variant of the "Fused Attention" page: q, k fp16/bf16
+    ``[B,H,L,D]`` CPU tensors, ``vt`` the transposed V as float8 e5m2
+    ``[B,H,D,L]`` (a ``torch.uint8`` or ``torch.float8_e5m2`` CPU tensor).
+    Returns ``(O, lse, slack)`` as float64 numpy arrays; ``slack`` bounds, per
+    row, the change of O when p values lying at a rounding tie of e5m2 round to
+    the other neighbour."""
+    qb, dt = _bits(q)
+    kb, dtk = _bits(k)
+    if dt != dtk:
+        raise TypeError("q and k must share one dtype")
+    B, H, L, D = (int(x) for x in q.shape)
+    if tuple(k.shape) != (B, H, L, D) or tuple(vt.shape) != (B, H, D, L):
+        raise ValueError("q, k must be [B,H,L,D] and vt [B,H,D,L]")
+    import torch
+    vb = np.ascontiguousarray(vt.detach().cpu().contiguous().view(torch.uint8).numpy())
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    scale = float(np.float32(sm_scale))
+    if rows is None:
+        rp, nrows = None, 0
+        O = np.empty((B, H, L, D), dtype=np.float64)
+        lse = np.empty((B, H, L), dtype=np.float64)
+        slack = np.empty((B, H, L), dtype=np.float64)
+    else:
+        ra = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        rp, nrows = ra.ctypes.data, int(ra.size)
+        O = np.empty((nrows, D), dtype=np.float64)
+        lse = np.empty((nrows,), dtype=np.float64)
+        slack = np.empty((nrows,), dtype=np.float64)
+    rc = load(mutant).attn_oracle_fp8v(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, dt, B, H, L, D, int(mask_kind),
+        int(block_size), scale, rp, nrows, O.ctypes.data, lse.ctypes.data, slack.ctypes.data,
+        int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
+    return O, lse, slack

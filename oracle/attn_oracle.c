@@ -32,6 +32,9 @@
  *
  * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake; the
  * CPU tests build every mutant and check that the pins catch each of them.
+ *
+ * attn_oracle_fp8v (at the end) is the page's FP8 variant, which is not the
+ * plain definition above: see its comment.
  */
 #include <math.h>
 #include <stdint.h>
@@ -220,6 +223,188 @@ int attn_oracle(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                     O + (size_t)t * D, lse + t);
         }
         free(qs); free(ks); free(vs); free(s);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ fp8 P.V
+ *
+ * The "Fused Attention" page's FP8 variant: V is given in float8 e5m2 and
+ * stored transposed ([B, H, D, L], keys innermost: the page notes that an
+ * e5m2 V is transposed), P is cast to e5m2 before P.V (`p.to(tl.float8e5)`),
+ * and the softmax denominator sums the unrounded p (`l_ij = tl.sum(p, 1)`).
+ * The result then depends on where P is rounded, so this function follows the
+ * page's tiled algorithm rather than the definition: key tiles of 128 keys
+ * from key 0, taken in order; per tile the running max m_new = max(m, tile
+ * max), p = exp(s - m_new) rounded to e5m2 for the P.V product, acc and l
+ * rescaled by exp(m - m_new).  Tiles without an attended key are skipped (they
+ * would change nothing).
+ */
+
+/* float8 e5m2 -> double: 1 sign bit, 5 exponent bits (bias 15), 2 fraction
+ * bits. */
+static double widen_e5m2(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1f;
+    int f = b & 3;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -16);               /* subnormal: f/4 * 2^-14 */
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(4 + f), e - 17);      /* (1 + f/4) * 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+double attn_oracle_widen_e5m2(uint8_t b)
+{
+    return widen_e5m2(b);
+}
+
+/* Round a finite x >= 0 to e5m2: nearest, ties to even, saturating at the
+ * largest finite value 57344.  *quantum receives the spacing of e5m2 values
+ * around x (the step a rounding decision spans). */
+static double round_e5m2(double x, double *quantum)
+{
+    double qv;
+    if (x < 0x1p-14) {
+        qv = 0x1p-16;                              /* subnormal spacing */
+    } else {
+        int ex;
+        frexp(x, &ex);                             /* x in [2^(ex-1), 2^ex) */
+        qv = ldexp(1.0, ex - 1 - 2);               /* 2 fraction bits */
+    }
+    if (quantum) *quantum = qv;
+#if ORACLE_MUTANT == 11
+    double r = floor(x / qv) * qv;                 /* planted: truncation */
+#else
+    double r = nearbyint(x / qv) * qv;             /* default rounding: ties to even */
+#endif
+    return r > 57344.0 ? 57344.0 : r;
+}
+
+double attn_oracle_round_e5m2(double x)
+{
+    return round_e5m2(x, NULL);
+}
+
+/* One query row of the FP8 variant.  q, k: the (b,h) slice [L, D] widened to
+ * fp64; vt: the (b,h) slice of V^T [D, L] as e5m2 bytes.  s: scratch of L.
+ * *slack receives a bound on how far a computation of p that differs from
+ * this one in the last bits of single precision can move O (a p within a
+ * relative 5e-5 of a rounding tie may round to either neighbour). */
+static void one_row_fp8v(const double *q, const double *k, const uint8_t *vt, long L, long D, long i,
+                         int mask_kind, long bs, double sm_scale, double *s, double *o, double *lse,
+                         double *slack)
+{
+    const double *qi = q + i * D;
+    double m = -INFINITY, l = 0.0, tie = 0.0;
+    for (long d = 0; d < D; ++d) o[d] = 0.0;
+    for (long t0 = 0; t0 < L; t0 += 128) {
+        const long t1 = t0 + 128 < L ? t0 + 128 : L;
+        double mt = -INFINITY;
+        int any = 0;
+        for (long j = t0; j < t1; ++j) {
+            if (!attended(i, j, mask_kind, bs)) continue;
+            double dot = 0.0;
+            for (long d = 0; d < D; ++d) dot += qi[d] * k[j * D + d];
+            s[j] = sm_scale * dot;
+            if (s[j] > mt) mt = s[j];
+            any = 1;
+        }
+        if (!any) continue;
+        const double m_new = mt > m ? mt : m;
+        const double alpha = exp(m - m_new);           /* 0 on the first tile */
+        for (long d = 0; d < D; ++d) o[d] *= alpha;
+        l *= alpha;
+        tie *= alpha;
+        for (long j = t0; j < t1; ++j) {
+            if (!attended(i, j, mask_kind, bs)) continue;
+            const double p = exp(s[j] - m_new);
+            double qv;
+            const double p8 = round_e5m2(p, &qv);
+#if ORACLE_MUTANT == 12
+            l += p8;                                   /* planted: sums the rounded p */
+#else
+            l += p;
+#endif
+            double vmax = 0.0;
+            for (long d = 0; d < D; ++d) {
+#if ORACLE_MUTANT == 13
+                const double vj = widen_e5m2(vt[j * D + d]);   /* planted: V read untransposed */
+#else
+                const double vj = widen_e5m2(vt[d * L + j]);
+#endif
+                o[d] += p8 * vj;
+                if (fabs(vj) > vmax) vmax = fabs(vj);
+            }
+            /* a tie within a relative 5e-5 of p: single-precision scores and
+             * exponentials may round to the other neighbour */
+            const double frac = p / qv - floor(p / qv);
+            if (fabs(frac - 0.5) < 5e-5 * (p / qv)) tie += qv * vmax;
+        }
+        m = m_new;
+    }
+    for (long d = 0; d < D; ++d) o[d] /= l;
+    *lse = m + log(l);
+    *slack = tie / l;
+}
+
+/*
+ * FP8 variant on Q, K as fp16/bf16 bits ([B,H,L,D]) and V^T as e5m2 bytes
+ * ([B,H,D,L]).  Same row selection and outputs as attn_oracle, plus slack
+ * ([B,H,L] or [nrows]): per row, the tie bound described above.
+ * Returns 0, or -1 on an argument error.
+ */
+int attn_oracle_fp8v(const uint16_t *q, const uint16_t *k, const uint8_t *vt, int dtype, long B, long H,
+                     long L, long D, int mask_kind, long bs, double sm_scale, const long *rows, long nrows,
+                     double *O, double *lse, double *slack, int nthreads)
+{
+    if (B < 0 || H < 0 || L < 0 || D <= 0) return -1;
+    if (mask_kind < OR_DENSE || mask_kind > OR_BLOCK_DIAG) return -1;
+    if (mask_kind == OR_BLOCK_DIAG && (bs <= 0 || (L > 0 && L % bs != 0))) return -1;
+    if (dtype != OR_F16 && dtype != OR_BF16) return -1;
+    const long BH = B * H;
+    const long total = rows ? nrows : BH * L;
+    if (total == 0) return 0;
+    if (rows)
+        for (long r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= BH * L) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double *qs = malloc(sizeof(double) * L * D);
+        double *ks = malloc(sizeof(double) * L * D);
+        double *s = malloc(sizeof(double) * (L > 0 ? L : 1));
+        long cur_bh = -1;
+        if (!qs || !ks || !s) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long t = 0; t < total; ++t) {
+            if (err) continue;
+            long r = rows ? rows[t] : t;
+            long bh = r / L, i = r % L;
+            if (bh != cur_bh) {
+                const size_t base = (size_t)bh * L * D;
+                for (long e = 0; e < L * D; ++e) {
+                    qs[e] = attn_oracle_widen(q[base + e], dtype);
+                    ks[e] = attn_oracle_widen(k[base + e], dtype);
+                }
+                cur_bh = bh;
+            }
+            one_row_fp8v(qs, ks, vt + (size_t)bh * D * L, L, D, i, mask_kind, bs, sm_scale, s,
+                         O + (size_t)t * D, lse + t, slack + t);
+        }
+        free(qs); free(ks); free(s);
     }
     return err ? -1 : 0;
 }

@@ -340,3 +340,136 @@ def test_page_fixture_matches_workload_table():
         fx = json.load(f)["fused_attention_test_matrix"]
     names = {torch.float16: "fp16", torch.bfloat16: "bf16"}
     assert [list(c[:4]) + [names[c[4]]] for c in PAGE_TEST_MATRIX] == fx["cases_Z_H_N_D_dtype"]
+
+
+# ------------------------------------------------------ FP8 P.V variant pins
+
+def _e5m2_values():
+    """Every finite non-negative e5m2 value, from the format's definition."""
+    vals = []
+    for e in range(31):
+        for f in range(4):
+            vals.append(math.ldexp(f, -16) if e == 0 else math.ldexp(4 + f, e - 17))
+    return sorted(set(vals))
+
+
+def _fp8_pin_top_byte_of_f16(mutant):
+    """e5m2 is the upper byte of IEEE binary16: widening byte b equals widening
+    the half-precision pattern b << 8."""
+    for b in range(256):
+        w8 = oracle.widen_e5m2(b, mutant=mutant)
+        w16 = oracle.widen(b << 8, oracle.F16, mutant=mutant)
+        assert (math.isnan(w8) and math.isnan(w16)) or w8 == w16, (b, w8, w16)
+
+
+def _fp8_pin_rounding_brute_force(mutant):
+    """Rounding to e5m2 is to the nearest value, ties to the even fraction
+    (brute force over every value), and saturates at 57344; it agrees with
+    torch's float8_e5m2 conversion."""
+    vals = _e5m2_values()
+    g = np.random.default_rng(3)
+    xs = list(np.exp(g.uniform(math.log(1e-6), math.log(5e4), size=400)))
+    xs += [(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])][::3]        # exact ties
+    for x in xs:
+        r = oracle.round_e5m2(x, mutant=mutant)
+        best = min(abs(v - x) for v in vals)
+        assert abs(r - x) == best, (x, r, best)
+        cands = [v for v in vals if abs(v - x) == best]
+        if len(cands) == 2:                                              # a tie: even fraction
+            even = [v for v in cands if (int(v / (math.ldexp(1, math.frexp(v)[1] - 3) if v >= 2 ** -14
+                                                   else 2 ** -16)) % 2) == 0]
+            assert r in even, (x, r, cands)
+        t = float(torch.tensor([x], dtype=torch.float64).to(torch.float8_e5m2).double())
+        assert r == t, (x, r, t)
+    assert oracle.round_e5m2(60000.0, mutant=mutant) == 57344.0
+
+
+def _fp8_run(mutant, q, k, vt, mask=DENSE, bs=0, scale=1.0):
+    return oracle.attention_fp8v(q, k, vt, mask, bs, scale, nthreads=2, mutant=mutant)
+
+
+def _fp8_pin_uniform_scores(mutant):
+    """Q = 0: every p is exactly 1 (exact in e5m2), so O is the plain mean of
+    the attended V rows and lse = ln(number attended), for every mask."""
+    B, H, L, D = 1, 2, 256, 8
+    g = torch.Generator().manual_seed(4)
+    q = torch.zeros(B, H, L, D, dtype=torch.float16)
+    k = torch.randn(B, H, L, D, generator=g).to(torch.float16)
+    vt = (torch.randn(B, H, D, L, generator=g) * 2).to(torch.float8_e5m2)
+    v = vt.double().transpose(-1, -2)                                     # [B,H,L,D]
+    for mask, bs in ((DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 64)):
+        O, lse, _ = _fp8_run(mutant, q, k, vt, mask, bs)
+        M = _mask_matrix(L, mask, bs).double()
+        n = M.sum(1)
+        want = torch.einsum("ij,bhjd->bhid", M, v) / n[None, None, :, None]
+        assert np.abs(O - want.numpy()).max() <= 1e-12
+        assert np.abs(lse - np.log(n.numpy())[None, None]).max() <= 1e-12
+
+
+def _fp8_pin_rounded_weights(mutant):
+    """Two keys, scores 0 and -0.05: p = (1, e^-0.05 = 0.951), rounded to e5m2
+    (1, 1); O = (1 v0 + 1 v1) / (1 + 0.951) -- the denominator sums the
+    unrounded p (the page's l_ij = sum(p))."""
+    q = torch.ones(1, 1, 2, 1, dtype=torch.float16)
+    k = torch.tensor([0.0, -0.05], dtype=torch.float16).view(1, 1, 2, 1)
+    vt = torch.tensor([2.0, 4.0]).to(torch.float8_e5m2).view(1, 1, 1, 2)
+    O, lse, _ = _fp8_run(mutant, q, k, vt)
+    s1 = float(k[0, 0, 1, 0])
+    p1 = math.exp(s1)
+    p1r = float(torch.tensor([p1], dtype=torch.float64).to(torch.float8_e5m2).double())
+    want = (1.0 * 2.0 + p1r * 4.0) / (1.0 + p1)
+    assert p1r == 1.0
+    for r in range(2):
+        assert abs(O[0, 0, r, 0] - want) <= 1e-12, (O[0, 0, r, 0], want)
+        assert abs(lse[0, 0, r] - math.log(1.0 + p1)) <= 1e-12
+
+
+def _fp8_pin_running_max_across_tiles(mutant):
+    """The page rounds P against the running max of the key tiles seen so far:
+    key 0 (tile 0, score 0) gets p = 1 when its tile is processed and is only
+    rescaled afterwards by exp(0 - 0.6), while the definition (max over all keys
+    first) would round e^-0.6 = 0.549 to 0.5.  Every other key scores -30
+    (p < 2^-17, rounded to 0)."""
+    L = 256
+    q = torch.ones(1, 1, L, 1, dtype=torch.float16)
+    kk = torch.full((L,), -30.0)
+    kk[0] = 0.0
+    kk[128] = 0.6
+    k = kk.to(torch.float16).view(1, 1, L, 1)
+    vv = torch.zeros(L)
+    vv[0], vv[128] = 2.0, 8.0
+    vt = vv.to(torch.float8_e5m2).view(1, 1, 1, L)
+    O, _, _ = _fp8_run(mutant, q, k, vt)
+    s128 = float(k[0, 0, 128, 0])
+    a = math.exp(0.0 - s128)
+    tiny = (L - 2) * math.exp(-30.0 - s128)
+    want = (a * 1.0 * 2.0 + 1.0 * 8.0) / (a + 1.0 + tiny)
+    assert abs(O[0, 0, 0, 0] - want) <= 1e-9, (O[0, 0, 0, 0], want)
+
+
+FP8_PINS = [_fp8_pin_top_byte_of_f16, _fp8_pin_rounding_brute_force, _fp8_pin_uniform_scores,
+            _fp8_pin_rounded_weights, _fp8_pin_running_max_across_tiles]
+
+
+@pytest.mark.parametrize("pin", FP8_PINS, ids=lambda f: f.__name__)
+def test_fp8_pins(pin):
+    pin(0)
+
+
+FP8_MUTANTS = {
+    11: "e5m2 rounding truncates",
+    12: "denominator sums the rounded p",
+    13: "V read untransposed",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(FP8_MUTANTS), ids=lambda m: FP8_MUTANTS[m].replace(" ", "_"))
+def test_fp8_planted_mistakes_are_caught(mutant):
+    caught = []
+    for pin in FP8_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(mutant)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {mutant}: {FP8_MUTANTS[mutant]}"
