@@ -276,40 +276,47 @@ __device__ __forceinline__ void mask_half(uint32_t (&v)[64], int base, int rel_l
             v[c] = __float_as_uint(fill);
 }
 
-// max (or min) of 64 raw scores with three-input min/max, four chains.
+// max (or min) of 64 raw scores with three-input min/max, four chains: keys
+// 0..7 seed the chains, keys 8..63 are taken eight at a time.
 __device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool want_max) {
     float a[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] = __uint_as_float(v[e]);
     if (want_max) {
 #pragma unroll
-        for (int c = 4; c < 64; c += 8)
+        for (int e = 0; e < 4; ++e) a[e] = fmaxf(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+#pragma unroll
+        for (int c = 8; c < 64; c += 8)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 a[e] = fmax3(a[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
-        return fmaxf(fmax3(a[0], a[1], a[2]), a[3]);
+        return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
     }
 #pragma unroll
-    for (int c = 4; c < 64; c += 8)
+    for (int e = 0; e < 4; ++e) a[e] = fminf(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+#pragma unroll
+    for (int c = 8; c < 64; c += 8)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             a[e] = fmin3(a[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
-    return fminf(fmin3(a[0], a[1], a[2]), a[3]);
+    return fminf(fminf(a[0], a[1]), fminf(a[2], a[3]));
 }
 
-// max (or min) of 32 raw scores, two chains.
+// max (or min) of 32 raw scores, two chains: keys 0..3 seed them, keys 4..31
+// are taken four at a time.
 __device__ __forceinline__ float row_extreme32(const uint32_t *v, bool want_max) {
-    float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
     if (want_max) {
+        float a = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+        float b = fmaxf(__uint_as_float(v[2]), __uint_as_float(v[3]));
 #pragma unroll
-        for (int c = 2; c < 32; c += 4) {
+        for (int c = 4; c < 32; c += 4) {
             a = fmax3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
             b = fmax3(b, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
         }
         return fmaxf(a, b);
     }
+    float a = fminf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+    float b = fminf(__uint_as_float(v[2]), __uint_as_float(v[3]));
 #pragma unroll
-    for (int c = 2; c < 32; c += 4) {
+    for (int c = 4; c < 32; c += 4) {
         a = fmin3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
         b = fmin3(b, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
     }

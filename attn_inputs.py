@@ -96,6 +96,27 @@ def make_qkv(B: int, H: int, L: int, D: int, dtype: torch.dtype, seed: int = 42,
     return tuple(out)
 
 
+def make_qkv_far_below_zero(B: int, H: int, L: int, D: int, dtype: torch.dtype, sign: int = 1,
+                            seed: int = 5):
+    """Seeded Q, K, V and sm_scale with every scaled score near -200: head-dim 0
+    carries q0 = -sign*a and k0 = a with a^2 / sqrt(D) = 200, sm_scale is
+    sign / sqrt(D), and the other dims stay N(0, 1), which spreads the scores a
+    few units around -200.  With sign = -1 the scale is negative and the raw
+    scores large and positive."""
+    q, k, v = make_qkv(B, H, L, D, dtype, seed=seed)
+    a = math.sqrt(200.0 * math.sqrt(D))
+    q[..., 0] = -sign * a
+    k[..., 0] = a
+    return q, k, v, sign / math.sqrt(D)
+
+
 def make_workload_inputs(w: Workload):
     return make_qkv(w.B, w.H, w.L, w.D, w.dtype, w.seed, w.std)
 
+
+
+def make_vt_e5m2(v: torch.Tensor) -> torch.Tensor:
+    """The FP8 P.V variant's V input: ``v`` ([B,H,L,D], fp16/bf16) rounded to
+    float8 e5m2 (torch's conversion, round to nearest even) and transposed to
+    ``[B,H,D,L]`` (keys innermost), contiguous."""
+    return v.float().to(torch.float8_e5m2).transpose(-1, -2).contiguous()

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from attn_inputs import (BLOCK_DIAG, CAUSAL, DENSE, PAGE_TEST_MATRIX, WORKLOADS, make_qkv,
-                         make_workload_inputs)
+                         make_qkv_far_below_zero, make_workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -172,6 +172,22 @@ def test_large_scores_exercise_rescaling(af, mask, bs):
 def test_unusual_scales(af, scale):
     _full_case(af, 1, 2, 384, 128, CAUSAL, 0, torch.float16, scale=scale)
     _full_case(af, 1, 2, 256, 64, BLOCK_DIAG, 32, torch.float16, scale=scale)
+
+
+@pytest.mark.parametrize("D,dt", [(64, torch.float16), (128, torch.bfloat16), (256, torch.float16),
+                                  (96, torch.bfloat16)])
+@pytest.mark.parametrize("mask,bs", [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 64)])
+@pytest.mark.parametrize("sign", [1, -1])
+def test_scores_far_below_zero(af, D, dt, mask, bs, sign):
+    """Every attended score far below zero: the row max (the raw-score minimum
+    for a negative sm_scale) is near -200, far from 0, so any extreme that let a
+    stray 0 in would underflow every p of the row and leave l = 0.  O is then a
+    plain weighted mean of V, lse near -200."""
+    q, k, v, scale = make_qkv_far_below_zero(1, 2, 384, D, dt, sign)
+    o, lse = _run(af, q, k, v, mask, bs, scale)
+    O_ref, lse_ref = oracle.attention(q, k, v, mask, bs, scale)
+    assert lse_ref.max() < -150.0
+    _check(o, lse, O_ref, lse_ref, dt, f"D={D} mask={mask} sign={sign}")
 
 
 @pytest.mark.parametrize("case", PAGE_TEST_MATRIX, ids=str)
