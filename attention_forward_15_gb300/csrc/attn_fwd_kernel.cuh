@@ -276,51 +276,37 @@ __device__ __forceinline__ void mask_half(uint32_t (&v)[64], int base, int rel_l
             v[c] = __float_as_uint(fill);
 }
 
-// max (or min) of 64 raw scores with three-input min/max, four chains: keys
-// 0..7 seed the chains, keys 8..63 are taken eight at a time.
-__device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool want_max) {
+// max (or min) of N raw scores (N even, N >= 12) with three-input min/max in
+// four chains: keys 0..11 seed the chains three at a time, keys 12..N-1 join
+// them two at a time -- N/2 operations in all, the fewest three-input ops can do.
+template <int N>
+__device__ __forceinline__ float row_extreme_n(const uint32_t *v, bool want_max) {
+    static_assert(N % 2 == 0 && N >= 12, "row_extreme_n: N even, at least 12");
     float a[4];
     if (want_max) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = fmaxf(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        for (int e = 0; e < 4; ++e)
+            a[e] = fmax3(__uint_as_float(v[3 * e]), __uint_as_float(v[3 * e + 1]), __uint_as_float(v[3 * e + 2]));
 #pragma unroll
-        for (int c = 8; c < 64; c += 8)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                a[e] = fmax3(a[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
-        return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+        for (int c = 12; c < N; c += 2)
+            a[(c / 2) & 3] = fmax3(a[(c / 2) & 3], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+        return fmaxf(fmax3(a[0], a[1], a[2]), a[3]);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] = fminf(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+    for (int e = 0; e < 4; ++e)
+        a[e] = fmin3(__uint_as_float(v[3 * e]), __uint_as_float(v[3 * e + 1]), __uint_as_float(v[3 * e + 2]));
 #pragma unroll
-    for (int c = 8; c < 64; c += 8)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            a[e] = fmin3(a[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
-    return fminf(fminf(a[0], a[1]), fminf(a[2], a[3]));
+    for (int c = 12; c < N; c += 2)
+        a[(c / 2) & 3] = fmin3(a[(c / 2) & 3], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+    return fminf(fmin3(a[0], a[1], a[2]), a[3]);
 }
 
-// max (or min) of 32 raw scores, two chains: keys 0..3 seed them, keys 4..31
-// are taken four at a time.
+__device__ __forceinline__ float row_extreme64(const uint32_t (&v)[64], bool want_max) {
+    return row_extreme_n<64>(v, want_max);
+}
+
 __device__ __forceinline__ float row_extreme32(const uint32_t *v, bool want_max) {
-    if (want_max) {
-        float a = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
-        float b = fmaxf(__uint_as_float(v[2]), __uint_as_float(v[3]));
-#pragma unroll
-        for (int c = 4; c < 32; c += 4) {
-            a = fmax3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-            b = fmax3(b, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-        }
-        return fmaxf(a, b);
-    }
-    float a = fminf(__uint_as_float(v[0]), __uint_as_float(v[1]));
-    float b = fminf(__uint_as_float(v[2]), __uint_as_float(v[3]));
-#pragma unroll
-    for (int c = 4; c < 32; c += 4) {
-        a = fmin3(a, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-        b = fmin3(b, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-    }
-    return fminf(a, b);
+    return row_extreme_n<32>(v, want_max);
 }
 
 // p = exp2(s * sc - m) for a 64-key half (keys base..base+63 of the tile):
@@ -885,12 +871,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         mask_half(*reinterpret_cast<uint32_t(*)[64]>(sv), 0, rel_lo, rel_hi, fill);
                         mask_half(*reinterpret_cast<uint32_t(*)[64]>(sv + 64), 64, rel_lo, rel_hi, fill);
                     }
-                    float ext;
-                    {
-                        const float e1 = row_extreme64(*reinterpret_cast<const uint32_t(*)[64]>(sv), sc >= 0.f);
-                        const float e2 = row_extreme64(*reinterpret_cast<const uint32_t(*)[64]>(sv + 64), sc >= 0.f);
-                        ext = sc >= 0.f ? fmaxf(e1, e2) : fminf(e1, e2);
-                    }
+                    const float ext = row_extreme_n<BN>(sv, sc >= 0.f);
                     const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
                     if (t == 0) {
                         m_ref = m_tile;
