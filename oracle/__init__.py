@@ -161,8 +161,9 @@ def attention_fp8v(q, k, vt, mask_kind: int, block_size: int = 0, sm_scale: floa
     ``[B,H,L,D]`` CPU tensors, ``vt`` the transposed V as float8 e5m2
     ``[B,H,D,L]`` (a ``torch.uint8`` or ``torch.float8_e5m2`` CPU tensor).
     Returns ``(O, lse, slack)`` as float64 numpy arrays; ``slack`` bounds, per
-    row, the change of O when p values lying at a rounding tie of e5m2 round to
-    the other neighbour."""
+    row, the change of O when p values that lie within the error bound of a
+    single-precision computation of their exponent (dot-product rounding
+    included) from an e5m2 rounding tie round to the other neighbour."""
     qb, dt = _bits(q)
     kb, dtk = _bits(k)
     if dt != dtk:

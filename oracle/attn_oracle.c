@@ -291,10 +291,14 @@ double attn_oracle_round_e5m2(double x)
 }
 
 /* One query row of the FP8 variant.  q, k: the (b,h) slice [L, D] widened to
- * fp64; vt: the (b,h) slice of V^T [D, L] as e5m2 bytes.  s: scratch of L.
- * *slack receives a bound on how far a computation of p that differs from
- * this one in the last bits of single precision can move O (a p within a
- * relative 5e-5 of a rounding tie may round to either neighbour). */
+ * fp64; vt: the (b,h) slice of V^T [D, L] as e5m2 bytes.  s: scratch of 2L.
+ * *slack receives a bound on how far a single-precision computation of p can
+ * move O by rounding a p that lies near an e5m2 rounding tie to the other
+ * neighbour.  "Near" is the error bound of such a computation of the exponent
+ * s_j - m (natural-log units): the rounding of a D-term dot product, at most
+ * D * 2^-24 * sum_d |q_d k_d| scaled by |sm_scale| (the standard bound of a
+ * recursive sum), the rounding of the scaled score and of the subtraction of
+ * the max, 2^-23 * (|s_j| + |m|), and 5e-5 for an approximate exponential. */
 static void one_row_fp8v(const double *q, const double *k, const uint8_t *vt, long L, long D, long i,
                          int mask_kind, long bs, double sm_scale, double *s, double *o, double *lse,
                          double *slack)
@@ -308,9 +312,13 @@ static void one_row_fp8v(const double *q, const double *k, const uint8_t *vt, lo
         int any = 0;
         for (long j = t0; j < t1; ++j) {
             if (!attended(i, j, mask_kind, bs)) continue;
-            double dot = 0.0;
-            for (long d = 0; d < D; ++d) dot += qi[d] * k[j * D + d];
+            double dot = 0.0, absdot = 0.0;
+            for (long d = 0; d < D; ++d) {
+                dot += qi[d] * k[j * D + d];
+                absdot += fabs(qi[d] * k[j * D + d]);
+            }
             s[j] = sm_scale * dot;
+            s[L + j] = fabs(sm_scale) * absdot;
             if (s[j] > mt) mt = s[j];
             any = 1;
         }
@@ -340,10 +348,12 @@ static void one_row_fp8v(const double *q, const double *k, const uint8_t *vt, lo
                 o[d] += p8 * vj;
                 if (fabs(vj) > vmax) vmax = fabs(vj);
             }
-            /* a tie within a relative 5e-5 of p: single-precision scores and
-             * exponentials may round to the other neighbour */
+            /* p within the single-precision error of a tie (relative band
+             * delta, see above) may round to the other neighbour */
+            const double delta = (double)D * 0x1p-24 * s[L + j] +
+                                 0x1p-23 * (fabs(s[j]) + fabs(m_new)) + 5e-5;
             const double frac = p / qv - floor(p / qv);
-            if (fabs(frac - 0.5) < 5e-5 * (p / qv)) tie += qv * vmax;
+            if (fabs(frac - 0.5) < delta * (p / qv)) tie += qv * vmax;
         }
         m = m_new;
     }
@@ -382,7 +392,7 @@ int attn_oracle_fp8v(const uint16_t *q, const uint16_t *k, const uint8_t *vt, in
     {
         double *qs = malloc(sizeof(double) * L * D);
         double *ks = malloc(sizeof(double) * L * D);
-        double *s = malloc(sizeof(double) * (L > 0 ? L : 1));
+        double *s = malloc(sizeof(double) * (L > 0 ? 2 * L : 1));
         long cur_bh = -1;
         if (!qs || !ks || !s) {
 #pragma omp atomic write
