@@ -39,6 +39,10 @@ _SIGNATURES = {
     "attn_abi_version": (ctypes.c_int, []),
     "attn_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_int] * 6 +
                       [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_fp8v": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                     ctypes.c_int, ctypes.c_void_p]),
 }
 
 _lib = None
@@ -158,6 +162,37 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int = DENS
                                      dt, ctypes.c_void_p(s.cuda_stream))
     if rc:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, mask_kind: int = DENSE,
+             block_size: int = 0, sm_scale: float | None = None, out: torch.Tensor | None = None,
+             lse_out: torch.Tensor | None = None, return_lse: bool = True):
+    """``attn_fwd_fp8v``: the FP8 P.V variant.  q, k are fp16/bf16 ``[B,H,L,D]``
+    CUDA tensors; ``vt`` is V transposed, ``[B,H,D,L]``, as ``torch.float8_e5m2``
+    (or its bytes as ``torch.uint8``).  Returns ``(o, lse)`` like ``fwd``."""
+    lib = load_library()
+    for t in (q, k, vt):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("fwd_fp8v takes contiguous CUDA tensors")
+    B, H, L, D = (int(x) for x in q.shape)
+    if tuple(k.shape) != (B, H, L, D) or tuple(vt.shape) != (B, H, D, L):
+        raise ValueError("q, k must be [B,H,L,D] and vt [B,H,D,L]")
+    if vt.element_size() != 1:
+        raise ValueError("vt must be float8 e5m2 (or its uint8 bytes)")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty_like(q)
+    lse = (lse_out if lse_out is not None else
+           torch.empty((B, H, L), dtype=torch.float32, device=q.device)) if return_lse else None
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device)
+        rc = lib.attn_fwd_fp8v(q.data_ptr(), k.data_ptr(), vt.data_ptr(), o.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, B, H, L, D,
+                               int(mask_kind), int(block_size), float(sm_scale), _dtype_code(q.dtype),
+                               ctypes.c_void_p(s.cuda_stream))
+    if rc:
+        raise AttnError(rc, "attn_fwd_fp8v")
     return o, lse
 
 

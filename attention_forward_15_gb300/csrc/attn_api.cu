@@ -23,7 +23,7 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     unsigned int *status = nullptr;   // device status word written by timed-out waits
-    bool smem_attr[3][2] = {};        // per (head dim, dtype): dynamic smem attribute set
+    bool smem_attr[6][2] = {};        // per (kernel, dtype): dynamic smem attribute set
 };
 
 std::mutex g_mutex;
@@ -148,14 +148,30 @@ int encode_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype)
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <int D, bool BF16, bool PAIR>
+// 3-D tensor map over V^T as float8 e5m2 bytes, [BH, D, L] with keys innermost:
+// box = 128 keys (128 bytes) x `rows` head-dim rows, 128-byte swizzle; rows
+// past D read as zero.
+int encode_map_vt8(CUtensorMap *m, const void *ptr, int BH, int L, int D, int rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(D),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(L),
+                             static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D)};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool BF16, bool PAIR, bool FP8V = false>
 int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdParams prm, int dtype,
            cudaStream_t stream) {
     using C = Cfg<D, PAIR>;
-    auto kern = attn::attn_fwd_kernel<D, BF16, PAIR>;
+    auto kern = attn::attn_fwd_kernel<D, BF16, PAIR, FP8V>;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
-        bool &set = st.smem_attr[head_dim_index(D)][BF16 ? 1 : 0];
+        bool &set = st.smem_attr[head_dim_index(D) + (FP8V ? 3 : 0)][BF16 ? 1 : 0];
         if (!set) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM_BYTES) != cudaSuccess)
@@ -166,7 +182,9 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
     CUtensorMap tq, tk, tv;
     int rc = encode_map(&tq, q, prm.BH, prm.L, prm.d_out, dtype);
     if (rc == ATTN_OK) rc = encode_map(&tk, k, prm.BH, prm.L, prm.d_out, dtype);
-    if (rc == ATTN_OK) rc = encode_map(&tv, v, prm.BH, prm.L, prm.d_out, dtype);
+    if (rc == ATTN_OK)
+        rc = FP8V ? encode_map_vt8(&tv, v, prm.BH, prm.L, prm.d_out, D / C::EPT)
+                  : encode_map(&tv, v, prm.BH, prm.L, prm.d_out, dtype);
     if (rc != ATTN_OK) return rc;
     const int grid = prm.n_units < st.sms ? prm.n_units : st.sms;
     // Programmatic dependent launch: the CTAs may be scheduled while the
@@ -252,11 +270,20 @@ int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size, int
     return ATTN_OK;
 }
 
-int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
-             int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// attn_fwd and attn_fwd_fp8v: validation, plan, parameters and the launch of the
+// kernel for the head dim (FP8V: V given as e5m2 V^T).
+template <bool FP8V>
+int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+               int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
     int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
     if (rc != ATTN_OK) return rc;
     if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
+    // V^T rows are L bytes: TMA needs them to be a multiple of 16 bytes
+    if (FP8V && L % 16 != 0) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -288,15 +315,29 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     const bool bf16 = dtype == ATTN_BF16;
     switch (kernel_dim(D)) {
         case 64:
-            return bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
-                        : launch<64, false, true>(*st, q, k, v, prm, dtype, s);
+            return bf16 ? launch<64, true, true, FP8V>(*st, q, k, v, prm, dtype, s)
+                        : launch<64, false, true, FP8V>(*st, q, k, v, prm, dtype, s);
         case 128:
-            return bf16 ? launch<128, true, true>(*st, q, k, v, prm, dtype, s)
-                        : launch<128, false, true>(*st, q, k, v, prm, dtype, s);
+            return bf16 ? launch<128, true, true, FP8V>(*st, q, k, v, prm, dtype, s)
+                        : launch<128, false, true, FP8V>(*st, q, k, v, prm, dtype, s);
         default:
-            return bf16 ? launch<256, true, false>(*st, q, k, v, prm, dtype, s)
-                        : launch<256, false, false>(*st, q, k, v, prm, dtype, s);
+            return bf16 ? launch<256, true, false, FP8V>(*st, q, k, v, prm, dtype, s)
+                        : launch<256, false, false, FP8V>(*st, q, k, v, prm, dtype, s);
     }
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+             int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+    return fwd_common<false>(q, k, v, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, stream);
+}
+
+int attn_fwd_fp8v(const void *q, const void *k, const void *vt, void *o, float *lse, int B, int H, int L,
+                  int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+    return fwd_common<true>(q, k, vt, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, stream);
 }
 
 int attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,

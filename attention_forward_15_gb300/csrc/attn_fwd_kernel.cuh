@@ -106,6 +106,13 @@ struct Cfg {
     __device__ static constexpr uint32_t p_col(int b) {
         return SEP ? 256u + static_cast<uint32_t>(b) * 64u : s_col(b) + BN / 2;
     }
+    // FP8 P.V variant: P as e5m2, four keys per column (32 columns a tile), where
+    // it overwrites nothing still to be read: the P columns of its own (SEP),
+    // over S keys 96..127, which the softmax holds in registers (pair), or the
+    // upper half of a whole-row-in-registers S (single).
+    __device__ static constexpr uint32_t pf8_col(int b) {
+        return SEP ? p_col(b) : (PAIR ? s_col(b) + 96u : s_col(b) + 64u);
+    }
     __device__ static constexpr uint32_t o_col(int w) {
         return SEP ? 384u + static_cast<uint32_t>(w) * 64u
                    : 256u + (PAIR ? static_cast<uint32_t>(w) * D : 0u);
@@ -364,6 +371,65 @@ __device__ __forceinline__ void exp_chunk(const uint32_t *v, int base, int rel_l
     tmem_st16(dst, pk);
 }
 
+// exp_chunk for P in float8 e5m2 (the FP8 P.V variant): the 32 keys are
+// rounded four to a word and stored as 8 TMEM columns at `dst`.
+template <bool MASKED>
+__device__ __forceinline__ void exp_chunk8(const uint32_t *v, int base, int rel_lo, int rel_hi,
+                                           float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(neg_m, neg_m);
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        float4 pp;
+        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1])),
+                                     sc2, nm2);
+        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])),
+                                     sc2, nm2);
+        pp.x = ex2_approx(x0.x);
+        pp.y = ex2_approx(x0.y);
+        pp.z = ex2_approx(x1.x);
+        pp.w = ex2_approx(x1.y);
+        if constexpr (MASKED) {
+            const unsigned width = static_cast<unsigned>(rel_hi - rel_lo);
+            const int c0 = base + 4 * e;
+            if (static_cast<unsigned>(c0 - rel_lo) >= width) pp.x = 0.f;
+            if (static_cast<unsigned>(c0 + 1 - rel_lo) >= width) pp.y = 0.f;
+            if (static_cast<unsigned>(c0 + 2 - rel_lo) >= width) pp.z = 0.f;
+            if (static_cast<unsigned>(c0 + 3 - rel_lo) >= width) pp.w = 0.f;
+        }
+        acc[(2 * e) & 3] = __fadd2_rn(acc[(2 * e) & 3], make_float2(pp.x, pp.y));
+        acc[(2 * e + 1) & 3] = __fadd2_rn(acc[(2 * e + 1) & 3], make_float2(pp.z, pp.w));
+        pk[e] = pack4_e5m2(pp.x, pp.y, pp.z, pp.w);
+    }
+    tmem_st8(dst, pk);
+}
+
+// The exponent chunk of keys [base, base+32) with P stored in the format of the
+// variant: 16-bit pairs at p16 + base/2, or e5m2 quads at p8 + base/4.
+template <bool BF16, bool MASKED, bool FP8V>
+__device__ __forceinline__ void exp_chunk_any(const uint32_t *v, int base, int rel_lo, int rel_hi, float sc,
+                                              float neg_m, float2 (&acc)[4], uint32_t p16, uint32_t p8) {
+    if constexpr (FP8V)
+        exp_chunk8<MASKED>(v, base, rel_lo, rel_hi, sc, neg_m, acc, p8 + static_cast<uint32_t>(base) / 4u);
+    else
+        exp_chunk<BF16, MASKED>(v, base, rel_lo, rel_hi, sc, neg_m, acc, p16 + static_cast<uint32_t>(base) / 2u);
+}
+
+// The same for a 64-key half held in one array.
+template <bool BF16, bool MASKED, bool FP8V>
+__device__ __forceinline__ void exp_half_any(const uint32_t (&v)[64], int base, int rel_lo, int rel_hi,
+                                             float sc, float neg_m, float2 (&acc)[4], uint32_t p16,
+                                             uint32_t p8) {
+    if constexpr (FP8V) {
+        exp_chunk8<MASKED>(v, base, rel_lo, rel_hi, sc, neg_m, acc, p8 + static_cast<uint32_t>(base) / 4u);
+        exp_chunk8<MASKED>(v + 32, base + 32, rel_lo, rel_hi, sc, neg_m, acc,
+                           p8 + static_cast<uint32_t>(base + 32) / 4u);
+    } else {
+        exp_half<BF16, MASKED>(v, base, rel_lo, rel_hi, sc, neg_m, acc, p16 + static_cast<uint32_t>(base) / 2u);
+    }
+}
+
 // exp_chunk without the mask and without the store: the 16 packed pairs stay
 // in `pk` for the caller to store later.
 template <bool BF16>
@@ -381,13 +447,41 @@ __device__ __forceinline__ void exp_pack(const uint32_t *v, float sc, float neg_
     }
 }
 
+// exp_pack for P in float8 e5m2: the 32 keys at v packed four to a word into
+// pk, for a later 8-column TMEM store.
+__device__ __forceinline__ void exp_pack8(const uint32_t *v, float sc, float neg_m, float2 (&acc)[4],
+                                          uint32_t (&pk)[8]) {
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1])),
+                                     sc2, nm2);
+        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])),
+                                     sc2, nm2);
+        const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+        const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+        acc[(2 * e) & 3] = __fadd2_rn(acc[(2 * e) & 3], p0);
+        acc[(2 * e + 1) & 3] = __fadd2_rn(acc[(2 * e + 1) & 3], p1);
+        pk[e] = pack4_e5m2(p0.x, p0.y, p1.x, p1.y);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <int D, bool BF16, bool PAIR>
+// FP8V: the FP8 P.V variant -- tmap_v maps V^T as float8 e5m2 bytes
+// ([B*H, D, L], keys innermost), P is rounded to e5m2 and P.V runs as a
+// kind::f8f6f4 MMA; the reference max is the exact running max (threshold 0),
+// so P is rounded against the same max as the page's recurrence.
+template <int D, bool BF16, bool PAIR, bool FP8V = false>
 __global__ void __launch_bounds__(Cfg<D, PAIR>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
     using C = Cfg<D, PAIR>;
+    constexpr float kThr = FP8V ? 0.f : kRescaleLog2;      // rescale threshold (log2 units)
+    // V^T rows per ring entry (FP8V) and the bytes of such an entry
+    constexpr int V8_ROWS = D / C::EPT;
+    constexpr int V8_BYTES = V8_ROWS * BN;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -459,6 +553,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // MMA issue helpers (called by a whole converged warp; one elected lane issues)
         constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
         constexpr uint32_t IDESC_PV = idesc_f16_f32acc(BF16, BM, D, true);
+        constexpr uint32_t IDESC_PV8 = idesc_e5m2_f32acc(BM, D);
         const uint32_t q_smem = s_base + C::OFF_Q;
         const uint32_t ring_smem = s_base + C::OFF_RING;
         // Descriptors advance by adding to their 16-byte-unit address field.
@@ -477,13 +572,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
         // consecutive 64-column boxes of V are C::CHUNK_BYTES apart (LBO).
         auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
-            const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, C::CHUNK_BYTES, 1024);
             const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
-            const uint32_t a_tmem = tmem + C::p_col(sbuf);
+            if constexpr (FP8V) {
+                // V^T rows of 128 keys (128 bytes, K-major); k-step kk covers keys
+                // [32kk, 32kk+32): 32 bytes into the swizzled row, 8 P columns
+                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, 16, 1024);
+                const uint32_t a_tmem = tmem + C::pf8_col(sbuf);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
-                       (accumulate || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / 32; ++kk)
+                    mma_ts_f8(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 2), IDESC_PV8,
+                              (accumulate || kk > 0) ? 1u : 0u);
+            } else {
+                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, C::CHUNK_BYTES, 1024);
+                const uint32_t a_tmem = tmem + C::p_col(sbuf);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
+                           (accumulate || kk > 0) ? 1u : 0u);
+            }
         };
 
     if (warp == C::WARP_TMA) {
@@ -524,8 +630,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         ok = wait_warp(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u,
                                        kSiteKvEmpty);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::ENTRY_BYTES);
                         const uint32_t dst = s_base + C::OFF_RING + slot * C::ENTRY_BYTES;
+                        if (FP8V && kind == 1) {
+                            // V^T: one box of 128 keys (128 bytes) x V8_ROWS head-dim rows
+                            mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), V8_BYTES);
+                            if (p.kv_keep)
+                                tma_load_3d_keep(dst, &tmap_v, j * BN, e * V8_ROWS, U.bh,
+                                                 bar(C::B_KVFULL + slot));
+                            else
+                                tma_load_3d(dst, &tmap_v, j * BN, e * V8_ROWS, U.bh, bar(C::B_KVFULL + slot));
+                            ++rc;
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::ENTRY_BYTES);
                         const CUtensorMap *m = kind == 0 ? &tmap_k : &tmap_v;
                         for (int c = 0; c < C::ENTRY_CHUNKS; ++c) {
                             if (p.kv_keep)
@@ -729,14 +846,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                            kSiteKvFullV);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES,
-                                                            C::CHUNK_BYTES, 1024);
                             const uint32_t d_tmem = tmem + C::o_col(0) + e * NV;
-                            const uint32_t a_tmem = tmem + C::p_col(b);
+                            if constexpr (FP8V) {
+                                constexpr uint32_t IDESC_PVE8 = idesc_e5m2_f32acc(BM, NV);
+                                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, 16, 1024);
+                                const uint32_t a_tmem = tmem + C::pf8_col(b);
 #pragma unroll
-                            for (int kk = 0; kk < BN / 16; ++kk)
-                                mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128),
-                                       IDESC_PVE, (t > 0 || kk > 0) ? 1u : 0u);
+                                for (int kk = 0; kk < BN / 32; ++kk)
+                                    mma_ts_f8(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 2),
+                                              IDESC_PVE8, (t > 0 || kk > 0) ? 1u : 0u);
+                            } else {
+                                const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES,
+                                                                C::CHUNK_BYTES, 1024);
+                                const uint32_t a_tmem = tmem + C::p_col(b);
+#pragma unroll
+                                for (int kk = 0; kk < BN / 16; ++kk)
+                                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128),
+                                           IDESC_PVE, (t > 0 || kk > 0) ? 1u : 0u);
+                            }
                             // this V entry is free once its part of P.V is done
                             mma_commit(bar(C::B_KVEMPTY + vslot));
                         }
@@ -846,6 +973,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_off + C::s_col(b);
                 const uint32_t p_addr = tmem + lane_off + C::p_col(b);
+                const uint32_t p8_addr = tmem + lane_off + C::pf8_col(b);   // FP8V
                 const bool masked = tile_masked(p, qt, j);
                 const int rel_lo = klo - j * BN, rel_hi = khi - j * BN;
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -875,7 +1003,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
                     if (t == 0) {
                         m_ref = m_tile;
-                    } else if (m_tile > m_ref + kRescaleLog2) {
+                    } else if (m_tile > m_ref + kThr) {
                         alpha = ex2_approx(m_ref - m_tile);
                         m_ref = m_tile;
                         rescale = true;
@@ -896,13 +1024,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     if (masked) {
 #pragma unroll
                         for (int c = 0; c < BN / 32; ++c)
-                            exp_chunk<BF16, true>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc,
-                                                  p_addr + 16 * c);
+                            exp_chunk_any<BF16, true, FP8V>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BN / 32; ++c)
-                            exp_chunk<BF16, false>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc,
-                                                   p_addr + 16 * c);
+                            exp_chunk_any<BF16, false, FP8V>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                     }
                 } else {
                     bool done = false;
@@ -927,18 +1053,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             tmem_wait_ld();
                             const float e1 = row_extreme32(lo, want_max);
                             ext = want_max ? fmaxf(ext, e1) : fminf(ext, e1);
-                            const bool fits = m_ref != -INFINITY && ext * sc <= m_ref + kRescaleLog2;
+                            const bool fits = m_ref != -INFINITY && ext * sc <= m_ref + kThr;
                             if (__all_sync(0xffffffffu, fits)) {
                                 neg_m = -m_ref;
                                 tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
-                                exp_chunk<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
-                                exp_chunk<BF16, false>(hi + 32, 96, rel_lo, rel_hi, sc, neg_m, acc,
-                                                       p_addr + 48);
+                                exp_chunk_any<BF16, false, FP8V>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                                exp_chunk_any<BF16, false, FP8V>(hi + 32, 96, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                                 tmem_wait_ld();
                                 tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(hi));
-                                exp_chunk<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                                exp_chunk_any<BF16, false, FP8V>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                                 tmem_wait_ld();
-                                exp_chunk<BF16, false>(hi, 32, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 16);
+                                exp_chunk_any<BF16, false, FP8V>(hi, 32, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                                 done = true;
                             }
                         }
@@ -954,7 +1079,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(sv));
                             tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
                             tmem_wait_ld();
-                            const float lim = m_ref + kRescaleLog2;
+                            const float lim = m_ref + kThr;
                             bool fits = m_ref != -INFINITY &&
                                         row_extreme64(sv, sc >= 0.f) * sc <= lim;
                             if (__all_sync(0xffffffffu, fits)) {
@@ -962,10 +1087,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                 // keys 0..63 from registers while keys 64..127 load; their
                                 // P waits in registers while the previous tile's P.V still
                                 // reads the P columns
-                                uint32_t pk0[16], pk1[16];
-                                exp_pack<BF16>(sv, sc, neg_m, acc, pk0);
+                                // (FP8V: e5m2 words, four keys each, in 8-column stores)
+                                uint32_t pk0[FP8V ? 8 : 16], pk1[FP8V ? 8 : 16];
+                                if constexpr (FP8V) exp_pack8(sv, sc, neg_m, acc, pk0);
+                                else exp_pack<BF16>(sv, sc, neg_m, acc, pk0);
                                 tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-                                exp_pack<BF16>(sv + 32, sc, neg_m, acc, pk1);
+                                if constexpr (FP8V) exp_pack8(sv + 32, sc, neg_m, acc, pk1);
+                                else exp_pack<BF16>(sv + 32, sc, neg_m, acc, pk1);
                                 // No TMEM load is left in flight across the wait below: its
                                 // slow path is a call, around which live registers may be
                                 // saved and restored, and the destination registers of a
@@ -975,8 +1103,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                 if (!ok) break;
                                 tc_fence_after();
                                 tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-                                tmem_st16(p_addr, pk0);
-                                tmem_st16(p_addr + 16, pk1);
+                                if constexpr (FP8V) {
+                                    tmem_st8(p8_addr, pk0);
+                                    tmem_st8(p8_addr + 8, pk1);
+                                } else {
+                                    tmem_st16(p_addr, pk0);
+                                    tmem_st16(p_addr + 16, pk1);
+                                }
                                 tmem_wait_ld();
                                 fits = row_extreme64(sv, sc >= 0.f) * sc <= lim;
                                 if (__all_sync(0xffffffffu, fits)) {
@@ -984,10 +1117,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                     tc_fence_before();
                                     __syncwarp();
                                     if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
-                                    exp_chunk<BF16, false>(sv, 64, rel_lo, rel_hi, sc, neg_m, acc,
-                                                           p_addr + 32);
-                                    exp_chunk<BF16, false>(sv + 32, 96, rel_lo, rel_hi, sc, neg_m, acc,
-                                                           p_addr + 48);
+                                    exp_chunk_any<BF16, false, FP8V>(sv, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                                    exp_chunk_any<BF16, false, FP8V>(sv + 32, 96, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                                     done = true;
                                 } else {
                                     // redo the whole tile: forget the first half's sums and
@@ -1024,7 +1155,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
                         if (t == 0) {
                             m_ref = m_tile;
-                        } else if (m_tile > m_ref + kRescaleLog2) {
+                        } else if (m_tile > m_ref + kThr) {
                             alpha = ex2_approx(m_ref - m_tile);
                             m_ref = m_tile;
                             rescale = true;
@@ -1047,9 +1178,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         // (the element-wise mask exists only in the masked instantiation,
                         // chosen once per tile)
                         if (masked)
-                            exp_half<BF16, true>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                            exp_half_any<BF16, true, FP8V>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                         else
-                            exp_half<BF16, false>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr + 32);
+                            exp_half_any<BF16, false, FP8V>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                         {
                             uint32_t lo[64];
                             tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
@@ -1062,9 +1193,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                 if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
                             }
                             if (masked)
-                                exp_half<BF16, true>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                                exp_half_any<BF16, true, FP8V>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                             else
-                                exp_half<BF16, false>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr);
+                                exp_half_any<BF16, false, FP8V>(lo, 0, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                         }
                     }
 

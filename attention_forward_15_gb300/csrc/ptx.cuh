@@ -167,6 +167,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// (warp) D[tmem] (+)= A[tmem] * B[smem desc], kind::f8f6f4 (8-bit operands,
+// K = 32 per instruction), one CTA.
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // (warp) arrive once on `bar` when every tcgen05 operation the issuing lane
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -197,6 +208,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+// 32 lanes x 32 bits, 8 consecutive columns.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -249,6 +268,16 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, int M, int N,
            | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
 
+// Instruction descriptor of a kind::f8f6f4 MMA with both operands float8 e5m2
+// (format code 1), both K-major, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e5m2_f32acc(int M, int N) {
+    return (1u << 4)                                   // D format: f32
+           | (1u << 7)                                  // A format: e5m2
+           | (1u << 10)                                 // B format: e5m2
+           | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
+}
+
 // ----------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -284,6 +313,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     else
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four fp32 values rounded to float8 e5m2 (nearest, saturating to the largest
+// finite value) in one word, a in the lowest byte.
+__device__ __forceinline__ uint32_t pack4_e5m2(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
     return r;
 }
 

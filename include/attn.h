@@ -151,6 +151,26 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
                      float sm_scale, int dtype, void *stream, unsigned int *status_out);
 
 /*
+ * attn_fwd_fp8v -- the FP8 P.V variant of the "Fused Attention" page: V is
+ * given in float8 e5m2 and transposed, P is rounded to e5m2 before the P.V
+ * product (which runs on the tensor cores in 8-bit), and the softmax
+ * denominator sums the unrounded weights.  P is rounded against the exact
+ * running max of the key tiles seen so far (128 keys a tile, in order), as in
+ * the page's recurrence.
+ *
+ *   vt          V^T: [B, H, D, L] float8 e5m2 bytes (keys innermost), device
+ *               memory, 16-byte aligned.
+ *   the rest    as for attn_fwd (q, k fp16/bf16 [B, H, L, D]; o in their type).
+ *
+ * L must be a multiple of 16 (each V^T row is L bytes, and TMA needs row
+ * strides in multiples of 16 bytes): other L give ATTN_ERR_UNSUPPORTED.
+ * Same errors, timeouts and stream behaviour as attn_fwd otherwise.
+ */
+int attn_fwd_fp8v(const void *q, const void *k, const void *vt, void *o, float *lse,
+                  int B, int H, int L, int D, int mask_kind, int block_size,
+                  float sm_scale, int dtype, void *stream);
+
+/*
  * attn_fwd_host -- the whole forward for inputs and outputs in HOST memory:
  * copies q, k, v to the device, runs attn_fwd, copies o (and lse) back and
  * synchronises `stream` before returning, so the host outputs are valid on

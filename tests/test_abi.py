@@ -75,6 +75,22 @@ def test_host_validation_before_any_cuda_call(lib):
     assert _fwd(lib, B=0, ptrs=(0, 0, 0, 0)) == 0
 
 
+def test_fp8v_host_validation(lib):
+    """attn_fwd_fp8v rejects its arguments on the host like attn_fwd, plus L not
+    a multiple of 16 (V^T rows must be 16-byte strides for TMA)."""
+    def f8(B=1, H=1, L=256, D=128, mask=0, bs=0, scale=0.1, dtype=0, ptrs=(16, 16, 16, 16)):
+        q, k, vt, o = (ctypes.c_void_p(p) if p else None for p in ptrs)
+        return lib.attn_fwd_fp8v(q, k, vt, o, None, B, H, L, D, mask, bs, scale, dtype, None)
+    assert f8(L=200) == 4
+    assert f8(L=8, ptrs=(0, 0, 0, 0)) == 4
+    assert f8(D=100) == 4
+    assert f8(mask=2, bs=48) == 3
+    assert f8(ptrs=(16, 16, 0, 16)) == 1
+    assert f8(ptrs=(16, 16, 24, 16)) == 5
+    assert f8(scale=float("nan")) == 8
+    assert f8(L=0, ptrs=(0, 0, 0, 0)) == 0
+
+
 def test_work_counts(lib):
     import attention_forward_15_gb300 as af
     f, b = af.work(4, 16, 1024, 64, af.DENSE)
