@@ -168,15 +168,18 @@ def make_device_inputs(w, dev):
                  .mul_(w.std).to(w.dtype) for _ in range(3))
 
 
-def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None):
-    """Device time per step (ms) of the forward on workload w.
+def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None, fp8v=False):
+    """Device time per step (ms) of the forward on workload w (``fp8v``: the
+    FP8 P.V variant, V given as e5m2 V^T).
 
     Steps rotate over enough input/output sets that each step reads its
     inputs from HBM, and are replayed from CUDA graphs (the launch loop is
     captured once: per-call host work such as tensor-map encoding is not in
     the timed region, only the kernels).  Returns (ms_per_step, info)."""
     q, k, v = make_device_inputs(w, dev)
-    per_set = 4 * q.numel() * q.element_size() + w.B * w.H * w.L * 4
+    if fp8v:
+        v = v.float().to(torch.float8_e5m2).transpose(-1, -2).contiguous()
+    per_set = 3 * q.numel() * q.element_size() + v.numel() * v.element_size() + w.B * w.H * w.L * 4
     nsets = rotation_sets(w, dev, per_set)
     sets = []
     for s in range(nsets):
@@ -186,7 +189,10 @@ def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None
 
     def step(i):
         qs, ks, vs, o, lse = sets[i % nsets]
-        af.fwd(qs, ks, vs, w.mask, w.block_size, w.sm_scale, out=o, lse_out=lse)
+        if fp8v:
+            af.fwd_fp8v(qs, ks, vs, w.mask, w.block_size, w.sm_scale, out=o, lse_out=lse)
+        else:
+            af.fwd(qs, ks, vs, w.mask, w.block_size, w.sm_scale, out=o, lse_out=lse)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
@@ -398,6 +404,17 @@ def main():
                               "tflops": round(f2 / (ms2 * 1e-3) / 1e12, 2),
                               "roofline_bound": rl["bound"], "roofline_frac": rl["frac"],
                               "achieved": rl["achieved"], "unit": rl["unit"]}
+    # The FP8 P.V variant (V as e5m2, P rounded to e5m2) on three workloads.
+    fp8_pv = {}
+    if not args.no_all:
+        for name in (w.name, "causal_b2h32l4096d128_bf16", "dense_b1h16l16384d256_bf16"):
+            ow = WORKLOADS[name]
+            f2, b2 = af.work(ow.B, ow.H, ow.L, ow.D, ow.mask, ow.block_size, ow.dtype)
+            steps2 = max(5, min(args.steps, int(2e12 / f2) + 5, 200))
+            ms2, _ = time_workload(af, ow, dev, steps2, 3, fp8v=True)
+            fp8_pv[name] = {"mask": MASK_NAMES[ow.mask], "ms": round(ms2, 4),
+                            "tflops": round(f2 / (ms2 * 1e-3) / 1e12, 2),
+                            "frac_of_bf16_peak": round(f2 / (ms2 * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
     if dist:
         dist.barrier()
     if rank != 0:
@@ -428,6 +445,7 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clocks,
         "per_workload": per_mask or None,
+        "fp8_pv_variant": fp8_pv or None,
     }
     out["cpu_baseline"] = None if args.lean else cpu_baseline(w)
     print(json.dumps(out), flush=True)
