@@ -85,6 +85,18 @@ def load(mutant: int = 0) -> ctypes.CDLL:
             ctypes.c_int, ctypes.c_long, ctypes.c_double,
             ctypes.c_void_p, ctypes.c_long,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.attn_oracle_bwd.restype = ctypes.c_int
+        lib.attn_oracle_bwd.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            ctypes.c_int, ctypes.c_long, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.attn_oracle_f64.restype = ctypes.c_int
+        lib.attn_oracle_f64.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            ctypes.c_int, ctypes.c_long, ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p]
         _libs[mutant] = lib
         return lib
 
@@ -194,3 +206,50 @@ def attention_fp8v(q, k, vt, mask_kind: int, block_size: int = 0, sm_scale: floa
     if rc != 0:
         raise ValueError("oracle rejected arguments")
     return O, lse, slack
+
+
+def _f64(t) -> np.ndarray:
+    """A CPU torch tensor (any float type) or numpy array as contiguous float64."""
+    if isinstance(t, np.ndarray):
+        return np.ascontiguousarray(t, dtype=np.float64)
+    return np.ascontiguousarray(t.detach().cpu().double().numpy())
+
+
+def attention_f64(q, k, v, mask_kind: int, block_size: int = 0, sm_scale: float = 1.0, mutant: int = 0):
+    """The forward on fp64 ``[B,H,L,D]`` inputs (no rounding of the inputs):
+    returns ``(O, lse)``."""
+    qa, ka, va = _f64(q), _f64(k), _f64(v)
+    B, H, L, D = qa.shape
+    O = np.empty_like(qa)
+    lse = np.empty((B, H, L))
+    rc = load(mutant).attn_oracle_f64(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, B, H, L, D,
+                                      int(mask_kind), int(block_size), float(sm_scale),
+                                      O.ctypes.data, lse.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
+    return O, lse
+
+
+def attention_bwd(q, k, v, dout, mask_kind: int, block_size: int = 0, sm_scale: float = 1.0,
+                  bounds: bool = False, nthreads: int = 0, mutant: int = 0):
+    """Gradients ``(dQ, dK, dV)`` of the attention forward for the output
+    gradient ``dout``, from the definition, in fp64 (inputs taken exactly as
+    given, 16-bit tensors widened).  With ``bounds``, also ``(bQ, bK, bV)``: per
+    element, the magnitudes that rounding P and dS to 16 bits and taking the
+    row term from a 16-bit O can act on (see ``attn_oracle.c``)."""
+    qa, ka, va, ga = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if not (qa.shape == ka.shape == va.shape == ga.shape) or qa.ndim != 4:
+        raise ValueError("q, k, v, dout must all be [B,H,L,D]")
+    B, H, L, D = qa.shape
+    dQ, dK, dV = np.empty_like(qa), np.empty_like(qa), np.empty_like(qa)
+    bq = bk = bv = None
+    if bounds:
+        bq, bk, bv = np.empty_like(qa), np.empty_like(qa), np.empty_like(qa)
+    ptr = lambda a: None if a is None else a.ctypes.data
+    rc = load(mutant).attn_oracle_bwd(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, ga.ctypes.data,
+                                      B, H, L, D, int(mask_kind), int(block_size), float(sm_scale),
+                                      dQ.ctypes.data, dK.ctypes.data, dV.ctypes.data,
+                                      ptr(bq), ptr(bk), ptr(bv), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
+    return (dQ, dK, dV, bq, bk, bv) if bounds else (dQ, dK, dV)

@@ -33,8 +33,9 @@
  * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake; the
  * CPU tests build every mutant and check that the pins catch each of them.
  *
- * attn_oracle_fp8v (at the end) is the page's FP8 variant, which is not the
- * plain definition above: see its comment.
+ * attn_oracle_fp8v is the page's FP8 variant, which is not the plain
+ * definition above: see its comment.  attn_oracle_bwd (at the end) is the
+ * gradient of the definition above by the chain rule: see its comment.
  */
 #include <math.h>
 #include <stdint.h>
@@ -417,4 +418,150 @@ int attn_oracle_fp8v(const uint16_t *q, const uint16_t *k, const uint8_t *vt, in
         free(qs); free(ks); free(s);
     }
     return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ backward
+ *
+ * Gradients of the masked softmax attention above with respect to q, k and v
+ * for an output gradient dO (the pages save q, k, v, O and the row statistic
+ * for a backward they do not define; this follows from the definition by the
+ * chain rule through the softmax), per head, for every row i and key j:
+ *
+ *   P[i,j]  = exp(s_ij - lse_i)   for j in A(i), 0 otherwise
+ *   dV[j,:] = sum_i P[i,j] dO[i,:]
+ *   dP[i,j] = sum_d dO[i,d] v[j,d]
+ *   Di      = sum_j P[i,j] dP[i,j]
+ *   dS[i,j] = P[i,j] (dP[i,j] - Di)
+ *   dQ[i,:] = sm_scale sum_j dS[i,j] k[j,:]
+ *   dK[j,:] = sm_scale sum_i dS[i,j] q[i,:]
+ *
+ * with s and lse as in one_row.  Inputs are fp64 [B,H,L,D] arrays (16-bit
+ * callers widen them first; the finite-difference pins perturb them).
+ *
+ * Also returned, per element, the magnitudes a computation that rounds P and
+ * dS to a 16-bit type and takes Di from a rounded O is sensitive to:
+ *   bV[j,d] = sum_i P[i,j] |dO[i,d]|
+ *   bK[j,d] = |sm_scale| sum_i (|dS[i,j]| + P[i,j] a_i) |q[i,d]|
+ *   bQ[i,d] = |sm_scale| sum_j (|dS[i,j]| + P[i,j] a_i) |k[j,d]|
+ * with a_i = sum_d |dO[i,d] O[i,d]|.  (Each may be NULL.)
+ */
+static void one_head_bwd(const double *q, const double *k, const double *v, const double *dO,
+                         long L, long D, int mask_kind, long bs, double sm_scale,
+                         double *dQ, double *dK, double *dV, double *bQ, double *bK, double *bV,
+                         double *s, double *P, double *dS, double *o)
+{
+    for (long e = 0; e < L * D; ++e) {
+        dQ[e] = dK[e] = dV[e] = 0.0;
+        if (bQ) bQ[e] = 0.0;
+        if (bK) bK[e] = 0.0;
+        if (bV) bV[e] = 0.0;
+    }
+    for (long i = 0; i < L; ++i) {
+        double lse;
+        one_row(q, k, v, L, D, i, mask_kind, bs, sm_scale, s, o, &lse);
+        const double *dOi = dO + i * D;
+        double Di = 0.0, ai = 0.0;
+        for (long d = 0; d < D; ++d) ai += fabs(dOi[d] * o[d]);
+        for (long j = 0; j < L; ++j) {
+            if (!attended(i, j, mask_kind, bs)) {
+                P[j] = 0.0;
+                dS[j] = 0.0;
+                continue;
+            }
+            P[j] = exp(s[j] - lse);
+            double dp = 0.0;
+            for (long d = 0; d < D; ++d) dp += dOi[d] * v[j * D + d];
+            dS[j] = dp;                                   /* dP for now */
+            Di += P[j] * dp;
+        }
+        for (long j = 0; j < L; ++j) {
+            if (P[j] == 0.0 && dS[j] == 0.0) continue;
+#if ORACLE_MUTANT == 21
+            dS[j] = P[j] * dS[j];                         /* planted: Di dropped */
+#else
+            dS[j] = P[j] * (dS[j] - Di);
+#endif
+        }
+        for (long j = 0; j < L; ++j) {
+            if (!attended(i, j, mask_kind, bs)) continue;
+            const double w = fabs(dS[j]) + P[j] * ai;
+            for (long d = 0; d < D; ++d) {
+#if ORACLE_MUTANT == 23
+                dV[i * D + d] += P[j] * dO[j * D + d];    /* planted: P transposed */
+#else
+                dV[j * D + d] += P[j] * dOi[d];
+#endif
+                dQ[i * D + d] += sm_scale * dS[j] * k[j * D + d];
+#if ORACLE_MUTANT == 22
+                dK[j * D + d] += dS[j] * q[i * D + d];    /* planted: scale dropped */
+#else
+                dK[j * D + d] += sm_scale * dS[j] * q[i * D + d];
+#endif
+                if (bV) bV[j * D + d] += P[j] * fabs(dOi[d]);
+                if (bQ) bQ[i * D + d] += fabs(sm_scale) * w * fabs(k[j * D + d]);
+                if (bK) bK[j * D + d] += fabs(sm_scale) * w * fabs(q[i * D + d]);
+            }
+        }
+    }
+}
+
+/* Backward over [B,H,L,D] fp64 inputs; outputs [B,H,L,D] fp64 (bQ, bK, bV may
+ * be NULL).  Heads are spread over OpenMP threads.  Returns 0, or -1 on an
+ * argument error. */
+int attn_oracle_bwd(const double *q, const double *k, const double *v, const double *dO, long B, long H,
+                    long L, long D, int mask_kind, long bs, double sm_scale, double *dQ, double *dK,
+                    double *dV, double *bQ, double *bK, double *bV, int nthreads)
+{
+    if (B < 0 || H < 0 || L < 0 || D <= 0) return -1;
+    if (mask_kind < OR_DENSE || mask_kind > OR_BLOCK_DIAG) return -1;
+    if (mask_kind == OR_BLOCK_DIAG && (bs <= 0 || (L > 0 && L % bs != 0))) return -1;
+    const long BH = B * H;
+    if (BH * L == 0) return 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = malloc(sizeof(double) * L);
+        double *P = malloc(sizeof(double) * L);
+        double *dS = malloc(sizeof(double) * L);
+        double *o = malloc(sizeof(double) * D);
+        if (!s || !P || !dS || !o) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            if (err) continue;
+            const size_t base = (size_t)bh * L * D;
+            one_head_bwd(q + base, k + base, v + base, dO + base, L, D, mask_kind, bs, sm_scale,
+                         dQ + base, dK + base, dV + base, bQ ? bQ + base : NULL, bK ? bK + base : NULL,
+                         bV ? bV + base : NULL, s, P, dS, o);
+        }
+        free(s); free(P); free(dS); free(o);
+    }
+    return err ? -1 : 0;
+}
+
+/* The forward of attn_oracle on fp64 inputs (for the backward's
+ * finite-difference pins): O [B,H,L,D] and lse [B,H,L]. */
+int attn_oracle_f64(const double *q, const double *k, const double *v, long B, long H, long L, long D,
+                    int mask_kind, long bs, double sm_scale, double *O, double *lse)
+{
+    if (B < 0 || H < 0 || L < 0 || D <= 0) return -1;
+    if (mask_kind < OR_DENSE || mask_kind > OR_BLOCK_DIAG) return -1;
+    if (mask_kind == OR_BLOCK_DIAG && (bs <= 0 || (L > 0 && L % bs != 0))) return -1;
+    double *s = malloc(sizeof(double) * (L > 0 ? L : 1));
+    if (!s) return -1;
+    for (long bh = 0; bh < B * H; ++bh) {
+        const size_t base = (size_t)bh * L * D;
+        for (long i = 0; i < L; ++i)
+            one_row(q + base, k + base, v + base, L, D, i, mask_kind, bs, sm_scale, s,
+                    O + base + i * D, lse + bh * L + i);
+    }
+    free(s);
+    return 0;
 }

@@ -473,3 +473,116 @@ def test_fp8_planted_mistakes_are_caught(mutant):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"no pin catches mutant {mutant}: {FP8_MUTANTS[mutant]}"
+
+
+# ----------------------------------------------------------------------------- backward pins
+# The backward is the gradient of the forward; its pins are facts that do not
+# come from the backward code: derivatives taken numerically from the forward,
+# a library's automatic differentiation of the same function, and invariants
+# of softmax attention.
+
+def _bwd_inputs(seed, L=10, D=6, H=2):
+    g = torch.Generator().manual_seed(seed)
+    return tuple(torch.randn((1, H, L, D), generator=g, dtype=torch.float64) for _ in range(4))
+
+
+BWD_MASKS = [(DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 5)]
+
+
+def _bwd_pin_finite_differences(mutant):
+    """<dX, E> against the central difference of sum(dO * O(X + eps E)) for a few
+    random directions E, X each of q, k, v; the forward is the oracle's own."""
+    scale = 0.7
+    for mask, bs in BWD_MASKS:
+        q, k, v, g = _bwd_inputs(3 + mask)
+        dq, dk, dv = oracle.attention_bwd(q, k, v, g, mask, bs, scale, mutant=mutant)
+        gn = g.numpy()
+
+        def loss(qq, kk, vv):
+            O, _ = oracle.attention_f64(qq, kk, vv, mask, bs, scale, mutant=mutant)
+            return float((O * gn).sum())
+
+        rng = np.random.default_rng(11 + mask)
+        eps = 1e-6
+        for which, grad in ((0, dq), (1, dk), (2, dv)):
+            for _ in range(3):
+                E = rng.standard_normal(q.shape)
+                args_p = [q.numpy(), k.numpy(), v.numpy()]
+                args_m = [q.numpy(), k.numpy(), v.numpy()]
+                args_p[which] = args_p[which] + eps * E
+                args_m[which] = args_m[which] - eps * E
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+                an = float((grad * E).sum())
+                assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (mask, which, fd, an)
+
+
+def _bwd_pin_torch_autograd(mutant):
+    """Library special case: torch's automatic differentiation of the same
+    masked softmax attention (additive -inf mask), fp64."""
+    scale = -0.45
+    for mask, bs in BWD_MASKS:
+        q, k, v, g = _bwd_inputs(30 + mask, L=20, D=8)
+        dq, dk, dv = oracle.attention_bwd(q, k, v, g, mask, bs, scale, mutant=mutant)
+        qq, kk, vv = (t.clone().requires_grad_() for t in (q, k, v))
+        s = (qq @ kk.transpose(-1, -2)) * scale
+        s = s.masked_fill(~_mask_matrix(20, mask, bs), float("-inf"))
+        (torch.softmax(s, dim=-1) @ vv).backward(g)
+        for a, b in ((dq, qq.grad), (dk, kk.grad), (dv, vv.grad)):
+            assert np.abs(a - b.numpy()).max() <= 1e-10
+
+
+def _bwd_pin_invariants(mutant):
+    """Adding one vector to every key leaves every row's softmax unchanged, so
+    the key gradients of a head sum to zero; the weights of a row sum to one,
+    so the value gradients of a head sum to the sum of the output gradients."""
+    for mask, bs in BWD_MASKS:
+        q, k, v, g = _bwd_inputs(50 + mask, L=20, D=5)
+        dq, dk, dv = oracle.attention_bwd(q, k, v, g, mask, bs, 0.9, mutant=mutant)
+        assert np.abs(dk.sum(axis=2)).max() <= 1e-12
+        assert np.abs(dv.sum(axis=2) - g.numpy().sum(axis=2)).max() <= 1e-12
+
+
+def _bwd_pin_block_size_one(mutant):
+    """Block size 1: every row attends only itself with weight 1, so dV = dO
+    and the softmax passes no gradient to q or k."""
+    q, k, v, g = _bwd_inputs(70, L=12, D=4)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, BLOCK_DIAG, 1, 0.3, mutant=mutant)
+    assert np.abs(dv - g.numpy()).max() == 0.0
+    assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0
+
+
+BWD_PINS = [_bwd_pin_finite_differences, _bwd_pin_torch_autograd, _bwd_pin_invariants,
+            _bwd_pin_block_size_one]
+
+
+@pytest.mark.parametrize("pin", BWD_PINS, ids=lambda f: f.__name__)
+def test_bwd_pins(pin):
+    pin(0)
+
+
+BWD_MUTANTS = {
+    21: "row term Di dropped from dS",
+    22: "sm_scale dropped from dK",
+    23: "P transposed in dV",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(BWD_MUTANTS), ids=lambda m: BWD_MUTANTS[m].replace(" ", "_"))
+def test_bwd_planted_mistakes_are_caught(mutant):
+    caught = []
+    for pin in BWD_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(mutant)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {mutant}: {BWD_MUTANTS[mutant]}"
+
+
+def test_bwd_bounds_dominate_gradients():
+    """The magnitude outputs bound what they describe: |dV| <= bV, and bK, bQ
+    are at least |dK|, |dQ| (triangle inequality)."""
+    q, k, v, g = _bwd_inputs(90, L=24, D=8)
+    dq, dk, dv, bq, bk, bv = oracle.attention_bwd(q, k, v, g, CAUSAL, 0, 0.6, bounds=True)
+    assert (np.abs(dv) <= bv + 1e-12).all()
+    assert (np.abs(dk) <= bk + 1e-12).all() and (np.abs(dq) <= bq + 1e-12).all()
