@@ -43,6 +43,10 @@ _SIGNATURES = {
                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                      ctypes.c_int, ctypes.c_void_p]),
+    "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_size_t] + [ctypes.c_int] * 6 +
+                 [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 3),
+    "attn_bwd_work": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_double)] * 2),
 }
 
 _lib = None
@@ -261,3 +265,55 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tens
     if rc:
         raise AttnError(rc, "attn_fwd_noalloc")
     return o, lse
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, mask_kind: int = DENSE, block_size: int = 0, sm_scale: float | None = None,
+        dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+        workspace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+    """``attn_bwd``: gradients ``(dq, dk, dv)`` of ``sum(dout * o)`` for the
+    forward ``fwd(q, k, v, mask_kind, block_size, sm_scale)`` that returned
+    ``(o, lse)``.  All CUDA tensors, contiguous, q/k/v/o/dout [B, H, L, D]
+    fp16/bf16 (D <= 128), lse float32 [B, H, L].  Asynchronous on ``stream``."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA [B, H, L, D] tensor")
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError(f"{name} must match q in shape, dtype and device")
+    B, H, L, D = (int(x) for x in q.shape)
+    if (not lse.is_cuda or tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32
+            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 CUDA [B, H, L] tensor")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    outs = []
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        t = torch.empty_like(q) if t is None else t
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous tensor like q")
+        outs.append(t)
+    need = int(lib.attn_bwd_workspace_size(B, H, L))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                          lse.data_ptr(), outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          B, H, L, D, int(mask_kind), int(block_size), float(sm_scale),
+                          _dtype_code(q.dtype), ctypes.c_void_p(s.cuda_stream))
+    if rc:
+        raise AttnError(rc, "attn_bwd")
+    return tuple(outs)
+
+
+def bwd_work(B: int, H: int, L: int, D: int, mask_kind: int, block_size: int = 0,
+             dtype: torch.dtype = torch.float16):
+    """(flops, bytes) of one attn_bwd (flops = 2.5 x the forward's)."""
+    f, b = ctypes.c_double(), ctypes.c_double()
+    rc = load_library().attn_bwd_work(B, H, L, D, mask_kind, block_size, _dtype_code(dtype),
+                                      ctypes.byref(f), ctypes.byref(b))
+    if rc:
+        raise AttnError(rc, "attn_bwd_work")
+    return f.value, b.value

@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include "attn.h"
+#include "attn_bwd_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 
 namespace {
@@ -24,6 +25,7 @@ struct DeviceState {
     int sms = 0;
     unsigned int *status = nullptr;   // device status word written by timed-out waits
     bool smem_attr[6][2] = {};        // per (kernel, dtype): dynamic smem attribute set
+    bool bwd_attr[2][2][2] = {};      // backward: per (head dim, dtype, dK/dV | dQ)
 };
 
 std::mutex g_mutex;
@@ -504,3 +506,159 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, voi
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Backward: attn_bwd_workspace_size, attn_bwd, attn_bwd_work.
+
+namespace {
+
+size_t bwd_workspace_bytes(long long BH, int L) {
+    const long long n_pad = static_cast<long long>((L + 127) / 128) * 128;
+    return static_cast<size_t>(2 * BH * n_pad) * sizeof(float);
+}
+
+template <int D, bool BF16, bool DQ>
+int launch_bwd(DeviceState &st, const CUtensorMap &f0, const CUtensorMap &f1, const CUtensorMap &r0,
+               const CUtensorMap &r1, const attn::BwdParams &prm, cudaStream_t stream) {
+    using C = attn::BwdCfg<D, DQ>;
+    auto kern = attn::attn_bwd_kernel<D, BF16, DQ>;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        bool &set = st.bwd_attr[D == 64 ? 0 : 1][BF16 ? 1 : 0][DQ ? 1 : 0];
+        if (!set) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+                cudaSuccess)
+                return ATTN_ERR_CUDA;
+            set = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(prm.BH) * static_cast<unsigned>(prm.n_t));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, f0, f1, r0, r1, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool BF16>
+int bwd_for_dim(DeviceState &st, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                const CUtensorMap &tg, attn::BwdParams prm, void *dq, void *dk, void *dv, cudaStream_t s) {
+    // dK/dV: fixed K, V; streamed Q, dO
+    prm.g0 = dk;
+    prm.g1 = dv;
+    int rc = launch_bwd<D, BF16, false>(st, tk, tv, tq, tg, prm, s);
+    if (rc != ATTN_OK) return rc;
+    // dQ: fixed Q, dO; streamed K, V
+    prm.g0 = dq;
+    prm.g1 = nullptr;
+    return launch_bwd<D, BF16, true>(st, tq, tg, tk, tv, prm, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(int B, int H, int L) {
+    if (B < 0 || H < 0 || L < 0) return 0;
+    return bwd_workspace_bytes(static_cast<long long>(B) * H, L);
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+             void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, int B, int H, int L, int D,
+             int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (D > 128) return ATTN_ERR_UNSUPPORTED;
+    if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
+    if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+        return ATTN_ERR_ALIGN;
+    const long long bh = static_cast<long long>(B) * H;
+    if (workspace_bytes < bwd_workspace_bytes(bh, L)) return ATTN_ERR_ARG;
+
+    DeviceState *st = nullptr;
+    rc = device_state(&st, nullptr);
+    if (rc != ATTN_OK) return rc;
+
+    attn::BwdParams prm = {};
+    prm.o = o;
+    prm.dout = dout;
+    prm.lse = lse;
+    prm.status = st->status;
+    prm.BH = static_cast<int>(bh);
+    prm.L = L;
+    prm.mask = mask_kind;
+    prm.bs = mask_kind == ATTN_MASK_BLOCK_DIAG ? block_size : 0;
+    prm.n_t = (L + 127) / 128;
+    prm.n_pad = prm.n_t * 128;
+    prm.lse2 = static_cast<float *>(workspace);
+    prm.delta = prm.lse2 + static_cast<size_t>(bh) * prm.n_pad;
+    prm.scale = sm_scale;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
+    prm.d_out = D;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bf16 = dtype == ATTN_BF16;
+    // Di, lse * log2(e), padded per head
+    {
+        const long long rows = bh * prm.n_pad;
+        long long blocks = (rows + 31) / 32;
+        const long long cap = static_cast<long long>(st->sms) * 16;
+        if (blocks > cap) blocks = cap;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = bf16 ? cudaLaunchKernelEx(&cfg, attn::attn_bwd_prep_kernel<true>, prm)
+                             : cudaLaunchKernelEx(&cfg, attn::attn_bwd_prep_kernel<false>, prm);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+    }
+    CUtensorMap tq, tk, tv, tg;
+    rc = encode_map(&tq, q, prm.BH, L, D, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tk, k, prm.BH, L, D, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tv, v, prm.BH, L, D, dtype);
+    if (rc == ATTN_OK) rc = encode_map(&tg, dout, prm.BH, L, D, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (kernel_dim(D) == 64)
+        return bf16 ? bwd_for_dim<64, true>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s)
+                    : bwd_for_dim<64, false>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s);
+    return bf16 ? bwd_for_dim<128, true>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s)
+                : bwd_for_dim<128, false>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s);
+}
+
+int attn_bwd_work(int B, int H, int L, int D, int mask_kind, int block_size, int dtype, double *flops,
+                  double *bytes) {
+    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (D > 128) return ATTN_ERR_UNSUPPORTED;
+    double f = 0.0;
+    rc = attn_fwd_work(B, H, L, D, mask_kind, block_size, dtype, &f, nullptr);
+    if (rc != ATTN_OK) return rc;
+    // five products of the forward's size (S, dP, dV, dK, dQ); the dQ kernel's
+    // second S and dP are not counted
+    if (flops) *flops = 2.5 * f;
+    // q, k, v, o, dO read and dq, dk, dv written once, lse read once
+    if (bytes) *bytes = (8.0 * 2.0 * D + 4.0) * static_cast<double>(B) * H * L;
+    return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,433 @@
+// Fused attention backward for sm_103a (GB300): gradients dQ, dK, dV of the
+// forward in attn_fwd_kernel.cuh for an output gradient dO, from the saved
+// per-row log-sum-exp (the "Fused Attention" page keeps q, k, v, O and that
+// statistic for a backward it does not define; this is the chain rule through
+// the softmax):
+//
+//   P    = exp(sm_scale q_i.k_j - lse_i)           (zero outside the mask)
+//   Di   = dO_i . O_i
+//   dV_j = sum_i P_ij dO_i          dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - Di)
+//   dQ_i = sm_scale sum_j dS_ij k_j     dK_j = sm_scale sum_i dS_ij q_i
+//
+// Three kernels, no atomics (results are deterministic):
+//   * attn_bwd_prep_kernel: Di per row, and per-head copies of lse*log2(e) and
+//     Di padded to whole 128-row tiles (padding rows: +inf and 0, so that rows
+//     past L give P = 0 wherever they are read);
+//   * attn_bwd_kernel<D, BF16, false> ("dK/dV"): one CTA per (head, key tile);
+//     K and V of the tile stay in shared memory while the query tiles that
+//     attend it stream through a ring; per query tile
+//         S^T = K Q^T, dP^T = V dO^T       (tcgen05, fp32 in tensor memory)
+//         P^T, dS^T in the compute warps   (one thread per key row)
+//         dV += P^T dO, dK += dS^T Q       (A operand from tensor memory)
+//   * attn_bwd_kernel<D, BF16, true> ("dQ"): one CTA per (head, query tile);
+//     Q and dO stay while the attended key tiles stream; per key tile
+//         S = Q K^T, dP = dO V^T, dS in the compute warps (one thread per query
+//         row), dQ += dS K.
+// Both are one template: a CTA holds a "fixed" pair of tiles (F0, F1) and
+// streams pairs (R0, R1); the products are S = F0 R0^T and dP = F1 R1^T in
+// either kernel, then (dK/dV) ACC0 += P R1 and, in both, ACC1 += dS R0.
+//
+// Tensor memory (512 columns): S at 0, dP at 128, ACC0 at 256, ACC1 at 256 + D.
+// P (16-bit pairs) is written over the first 64 columns of S and dS over the
+// first 64 of dP, as the columns are consumed; the next tile's S and dP are
+// issued after the products that read them, on the same in-order MMA pipe.
+// D is 64 or 128 (S, dP and two D-wide accumulators fill the 512 columns).
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+struct BwdParams {
+    const void *o;           // prep: forward output [BH, L, d_out] 16-bit
+    const void *dout;        // prep: output gradient [BH, L, d_out] 16-bit
+    const float *lse;        // prep: forward lse [BH, L] (natural log)
+    float *lse2;             // [BH, n_pad]: lse * log2(e), +inf past L
+    float *delta;            // [BH, n_pad]: Di, 0 past L
+    void *g0;                // dK/dV: dK, dQ: dQ   [BH, L, d_out] 16-bit
+    void *g1;                // dK/dV: dV           [BH, L, d_out] 16-bit
+    unsigned int *status;
+    int BH, L, mask, bs;
+    int n_t;                 // 128-row tiles per head
+    int n_pad;               // n_t * 128
+    float scale;             // sm_scale
+    float scale_log2;        // sm_scale * log2(e)
+    int d_out;               // head dim in memory (<= D of the kernel)
+};
+
+// ------------------------------------------------------------------ prep
+
+// Di = sum_d dO[i,d] O[i,d] (fp32) and lse2 = lse * log2(e) for every row of
+// every head, padded to n_pad rows.  Eight threads per row, 16 bytes each per
+// step, reduced by shuffles; grid-stride over rows.
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int sub = threadIdx.x & 7;
+    const long long rows = static_cast<long long>(p.BH) * p.n_pad;
+    const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x / 8);
+    for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 8) + (threadIdx.x >> 3); r < rows;
+         r += stride) {
+        const int bh = static_cast<int>(r / p.n_pad);
+        const int i = static_cast<int>(r % p.n_pad);
+        float acc = 0.f;
+        if (i < p.L) {
+            const size_t base = (static_cast<size_t>(bh) * p.L + i) * p.d_out;
+            const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.o) + base);
+            const uint4 *g4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) + base);
+            for (int c = sub; c < p.d_out / 8; c += 8) {
+                const uint4 a = o4[c], b = g4[c];
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = unpack2<BF16>(aw[e]), y = unpack2<BF16>(bw[e]);
+                    acc = fmaf(x.x, y.x, acc);
+                    acc = fmaf(x.y, y.y, acc);
+                }
+            }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (sub == 0) {
+            p.delta[r] = i < p.L ? acc : 0.f;
+            p.lse2[r] = i < p.L ? p.lse[static_cast<size_t>(bh) * p.L + i] * 1.4426950408889634f : INFINITY;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ dK/dV and dQ
+
+template <int D, bool DQ>
+struct BwdCfg {
+    static constexpr int CHUNKS = D / 64;               // 128-byte-wide TMA boxes per row
+    static constexpr int CHUNK_BYTES = 128 * 128;
+    static constexpr int TILE_BYTES = 128 * D * 2;
+    static constexpr int NS = D == 64 ? 3 : 2;          // ring stages of streamed pairs
+    static constexpr int THREADS = 192;                 // 4 compute warps, TMA warp, MMA warp
+    static constexpr int WARP_TMA = 4, WARP_MMA = 5;
+    static constexpr int VEC_BYTES = DQ ? 0 : 2 * 128 * 4;   // lse2 and Di of one query tile
+    static constexpr int OFF_FIX = 0;                        // F0 | F1
+    static constexpr int OFF_RING = 2 * TILE_BYTES;          // NS x (R0 | R1)
+    static constexpr int OFF_VEC = OFF_RING + NS * 2 * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_VEC + NS * VEC_BYTES;
+    static constexpr int B_FIX = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_SFULL = 1 + 2 * NS;
+    static constexpr int B_PFULL = B_SFULL + 1, B_DONE = B_PFULL + 1, B_DRAIN = B_DONE + 1;
+    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // [0]: TMEM base, [1]: abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC0 = 256, COL_ACC1 = 256 + D;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(D == 64 || D == 128, "backward head dim");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Streamed-tile range [lo, hi) of a CTA whose fixed tile is f: for dK/dV the
+// query tiles that attend key tile f, for dQ the key tiles query tile f
+// attends (tiles wholly outside the mask are left out).
+__device__ __forceinline__ void bwd_range(const BwdParams &p, bool dq, int f, int &lo, int &hi) {
+    if (p.mask == kMaskDense) {
+        lo = 0;
+        hi = p.n_t;
+    } else if (p.mask == kMaskCausal) {
+        lo = dq ? 0 : f;
+        hi = dq ? f + 1 : p.n_t;
+    } else {
+        // blocks are symmetric: the tiles meeting the blocks of tile f
+        const int r0 = f * 128;
+        const int r1 = min(r0 + 128, p.L);
+        const int blo = (r0 / p.bs) * p.bs;
+        const int bhi = ((r1 - 1) / p.bs + 1) * p.bs;
+        lo = blo / 128;
+        hi = (bhi + 127) / 128;
+    }
+}
+
+// dS (and P) of one 32-column chunk: rows are this thread's TMEM lane, columns
+// c0..c0+31 of the tile.  S, dP: fp32 raw scores and dP of the chunk.
+// Column-indexed (dK/dV) or row (dQ) lse2 / Di; `keep` masks (row, column).
+template <bool BF16, bool DQ, bool MASKED>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&S)[32], const uint32_t (&dP)[32], float sc,
+                                          float row_lse2, float row_delta, const float *col_lse2,
+                                          const float *col_delta, int c0, int mask, int bs, int L,
+                                          int row_idx, int col_base, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        float pv[2], dv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = c0 + 2 * e + h;
+            const float l2 = DQ ? row_lse2 : col_lse2[c];
+            const float dl = DQ ? row_delta : col_delta[c];
+            float pp = ex2_approx(fmaf(__uint_as_float(S[2 * e + h]), sc, -l2));
+            if constexpr (MASKED) {
+                // (query, key) of this element; keys past L are zero rows whose
+                // p could overflow when lse is very negative, so they are cut too
+                const int qi = DQ ? row_idx : col_base + c;
+                const int kj = DQ ? col_base + c : row_idx;
+                bool keep = kj < L;
+                if (mask == kMaskCausal) keep = keep && kj <= qi;
+                else if (mask == kMaskBlock) keep = keep && (kj / bs) == (qi / bs);
+                if (!keep) pp = 0.f;
+            }
+            pv[h] = pp;
+            dv[h] = pp * (__uint_as_float(dP[2 * e + h]) - dl);
+        }
+        pk[e] = pack2<BF16>(pv[0], pv[1]);
+        dk[e] = pack2<BF16>(dv[0], dv[1]);
+    }
+}
+
+template <int D, bool BF16, bool DQ>
+__global__ void __launch_bounds__(BwdCfg<D, DQ>::THREADS, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant__ CUtensorMap tm_f1,
+                const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
+                const BwdParams p) {
+    using C = BwdCfg<D, DQ>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + C::OFF_BAR;
+    auto bar = [&](int idx) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(idx); };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    const Ctl ctl{reinterpret_cast<volatile int *>(misc + 1), p.status};
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // unit of this CTA: (head, fixed tile); causal units heaviest first
+    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
+    const int rank = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));
+    const int f = (p.mask == kMaskCausal && DQ) ? p.n_t - 1 - rank : rank;
+    int lo, hi;
+    bwd_range(p, DQ, f, lo, hi);
+    const int n = hi - lo;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_FIX), 1);
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_PFULL), 4);       // one arrival per compute warp
+        mbar_init(bar(C::B_DONE), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::WARP_TMA && lane == 0) {
+        tma_prefetch_desc(&tm_f0);
+        tma_prefetch_desc(&tm_f1);
+        tma_prefetch_desc(&tm_r0);
+        tma_prefetch_desc(&tm_r1);
+    }
+    if (warp == C::WARP_MMA) {
+        tmem_alloc(s_base + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    griddep_wait();
+    griddep_launch_dependents();
+    constexpr uint32_t tmem = 0;
+    const bool tmem_ok = misc[0] == 0u;
+    if (!tmem_ok && threadIdx.x == 0) atomicCAS(p.status, 0u, kStatusTmem);
+    const int nn = tmem_ok ? n : 0;
+
+    auto wait_warp = [&](uint32_t bar_addr, uint32_t parity, unsigned site) -> bool {
+        const bool r = wait_bar(bar_addr, parity, ctl, site);
+        return __all_sync(0xffffffffu, r);
+    };
+
+    if (warp == C::WARP_TMA) {
+        // ================================================================ TMA producer
+        uint32_t issued = 0;          // streamed stages issued
+        bool fix_issued = false;
+        bool ok = true;
+        if (nn > 0) {
+            mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c) {
+                tma_load_3d(s_base + C::OFF_FIX + c * C::CHUNK_BYTES, &tm_f0, c * 64, f * 128, bh, bar(C::B_FIX));
+                tma_load_3d(s_base + C::OFF_FIX + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_f1, c * 64, f * 128, bh,
+                            bar(C::B_FIX));
+            }
+            fix_issued = true;
+        }
+        for (int t = 0; t < nn && ok; ++t) {
+            const int s = t % C::NS;
+            ok = wait_warp(bar(C::B_EMPTY + s), ((t / C::NS) & 1) ^ 1, kSiteKvEmpty);
+            if (!ok) break;
+            const int j = lo + t;
+            mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE_BYTES + C::VEC_BYTES);
+            const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE_BYTES;
+            for (int c = 0; c < C::CHUNKS; ++c) {
+                tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_r0, c * 64, j * 128, bh, bar(C::B_FULL + s));
+                tma_load_3d(dst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_r1, c * 64, j * 128, bh,
+                            bar(C::B_FULL + s));
+            }
+            if constexpr (!DQ) {
+                const size_t off = static_cast<size_t>(bh) * p.n_pad + static_cast<size_t>(j) * 128;
+                const uint32_t vdst = s_base + C::OFF_VEC + s * C::VEC_BYTES;
+                bulk_load_1d(vdst, p.lse2 + off, 512, bar(C::B_FULL + s));
+                bulk_load_1d(vdst + 512, p.delta + off, 512, bar(C::B_FULL + s));
+            }
+            ++issued;
+        }
+        if (*ctl.abort_flag) {
+            // stopping early: the copies already issued land before shared memory goes away
+            if (fix_issued) wait_slow(bar(C::B_FIX), 0, ctl, kSiteDrain, false);
+            const uint32_t first = issued > static_cast<uint32_t>(C::NS) ? issued - C::NS : 0u;
+            for (uint32_t t = first; t < issued; ++t)
+                wait_slow(bar(C::B_FULL + t % C::NS), (t / C::NS) & 1u, ctl, kSiteDrain, false);
+        }
+        __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+        // ================================================================ MMA issuer
+        constexpr uint32_t IDESC_SS = idesc_f16_f32acc(BF16, 128, 128, false);
+        constexpr uint32_t IDESC_ACC = idesc_f16_f32acc(BF16, 128, D, true);
+        const uint32_t f0 = s_base + C::OFF_FIX, f1 = f0 + C::TILE_BYTES;
+        // X = A B^T over the head dim: both K-major, k-step kk = head-dim
+        // columns [16kk, 16kk+16): box kk/4, 32-byte offset kk%4.
+        auto issue_ss = [&](uint32_t a, uint32_t b, uint32_t dcol) {
+            const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
+                mma_ss(tmem + dcol, ad + off, bd + off, IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+        };
+        // ACC += A(TMEM, 16-bit pairs) B, B MN-major: k-step kk = rows
+        // [16kk, 16kk+16) of B; its 64-column boxes are CHUNK_BYTES apart.
+        auto issue_acc = [&](uint32_t acol, uint32_t b, uint32_t dcol, bool accumulate) {
+            const uint64_t bd = sdesc_sw128(b, C::CHUNK_BYTES, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 128 / 16; ++kk)
+                mma_ts(tmem + dcol, tmem + acol + kk * 8, bd + static_cast<uint64_t>(kk * 128), IDESC_ACC,
+                       (accumulate || kk > 0) ? 1u : 0u);
+        };
+        bool ok = nn > 0;
+        if (ok) ok = wait_warp(bar(C::B_FIX), 0, kSiteQFull);
+        if (ok) ok = wait_warp(bar(C::B_FULL + 0), 0, kSiteKvFullK);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t r = s_base + C::OFF_RING;
+            issue_ss(f0, r, C::COL_S);
+            issue_ss(f1, r + C::TILE_BYTES, C::COL_DP);
+            mma_commit(bar(C::B_SFULL));
+        }
+        for (int t = 0; t < nn && ok; ++t) {
+            const int s = t % C::NS;
+            ok = wait_warp(bar(C::B_PFULL), t & 1, kSitePFull);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t r0 = s_base + C::OFF_RING + s * 2 * C::TILE_BYTES, r1 = r0 + C::TILE_BYTES;
+            if constexpr (!DQ) issue_acc(C::COL_S, r1, C::COL_ACC0, t > 0);     // dV += P^T dO
+            issue_acc(C::COL_DP, r0, C::COL_ACC1, t > 0);                        // dK += dS^T Q | dQ += dS K
+            mma_commit(bar(C::B_EMPTY + s));
+            if (t + 1 < nn) {
+                const int s2 = (t + 1) % C::NS;
+                ok = wait_warp(bar(C::B_FULL + s2), ((t + 1) / C::NS) & 1, kSiteKvFullK);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t q0 = s_base + C::OFF_RING + s2 * 2 * C::TILE_BYTES;
+                issue_ss(f0, q0, C::COL_S);
+                issue_ss(f1, q0 + C::TILE_BYTES, C::COL_DP);
+                mma_commit(bar(C::B_SFULL));
+            }
+        }
+        if (ok && nn > 0) mma_commit(bar(C::B_DONE));
+        // every MMA (and the arrivals its commits make) done before the CTA
+        // frees tensor memory and exits
+        mma_commit(bar(C::B_DRAIN));
+        wait_slow(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
+        __syncwarp();
+    } else {
+        // ================================================================ compute warps
+        const int row = warp * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int row_idx = f * 128 + row;                 // query (dQ) or key (dK/dV) index
+        const float sc = p.scale_log2;
+        float row_lse2 = 0.f, row_delta = 0.f;
+        if constexpr (DQ) {
+            row_lse2 = p.lse2[static_cast<size_t>(bh) * p.n_pad + row_idx];
+            row_delta = p.delta[static_cast<size_t>(bh) * p.n_pad + row_idx];
+        }
+        bool ok = true;
+        for (int t = 0; t < nn && ok; ++t) {
+            ok = wait_warp(bar(C::B_SFULL), t & 1, kSiteSFull);
+            if (!ok) break;
+            tc_fence_after();
+            const int s = t % C::NS;
+            const int j = lo + t;
+            const float *vec = reinterpret_cast<const float *>(smem + C::OFF_VEC + s * C::VEC_BYTES);
+            // tiles that cross the mask, and (dQ) a ragged last key tile
+            const bool masked = (p.mask == kMaskCausal && j == f) || (p.mask == kMaskBlock && (p.bs % 128) != 0) ||
+                                (DQ && (j + 1) * 128 > p.L);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(tmem + lane_off + C::COL_S + 32 * c, sv);
+                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * c, dpv);
+                tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+                if (masked)
+                    bwd_chunk<BF16, DQ, true>(sv, dpv, sc, row_lse2, row_delta, vec, vec + 128, 32 * c, p.mask,
+                                              p.bs, p.L, row_idx, j * 128, pk, dk);
+                else
+                    bwd_chunk<BF16, DQ, false>(sv, dpv, sc, row_lse2, row_delta, vec, vec + 128, 32 * c, p.mask,
+                                               p.bs, p.L, row_idx, j * 128, pk, dk);
+                // columns [16c, 16c+16) of S and dP were read in this or an earlier chunk
+                if constexpr (!DQ) tmem_st16(tmem + lane_off + C::COL_S + 16 * c, pk);
+                tmem_st16(tmem + lane_off + C::COL_DP + 16 * c, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_PFULL));
+        }
+        if (ok && nn > 0) ok = wait_warp(bar(C::B_DONE), 0, kSiteODone);
+        if (ok && nn > 0) {
+            tc_fence_after();
+            const bool row_valid = row_idx < p.L;
+            // ACC1 (dK or dQ, times sm_scale) to g0; dK/dV: ACC0 (dV) to g1
+#pragma unroll 1
+            for (int which = 0; which < (DQ ? 1 : 2); ++which) {
+                const uint32_t acol = which == 0 ? C::COL_ACC1 : C::COL_ACC0;
+                const float mul = which == 0 ? p.scale : 1.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(which == 0 ? p.g0 : p.g1) +
+                                                       ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out) * 2);
+#pragma unroll 1
+                for (int c = 0; c < D / 32 && 32 * c < p.d_out; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tmem + lane_off + acol + 32 * c, raw);
+                    tmem_wait_ld();
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * mul, __uint_as_float(raw[2 * e + 1]) * mul);
+                    if (row_valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            if (32 * c + 8 * v4 < p.d_out)
+                                dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
+                                                             w16[4 * v4 + 3]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace attn

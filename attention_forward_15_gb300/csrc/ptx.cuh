@@ -119,6 +119,17 @@ __device__ __forceinline__ void tma_load_3d_keep(uint32_t dst, const CUtensorMap
 
 // ------------------------------------------------------------------ tcgen05
 
+// (warp) 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), counted on the mbarrier's transaction bytes.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)
@@ -318,6 +329,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // Four fp32 values rounded to float8 e5m2 (nearest, saturating to the largest
 // finite value) in one word, a in the lowest byte.
+// Two 16-bit values of a 32-bit word (lower half first) widened to fp32.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        float lo, hi;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(w));
+        return make_float2(lo, hi);
+    }
+}
+
 __device__ __forceinline__ uint32_t pack4_e5m2(float a, float b, float c, float d) {
     uint32_t r;
     asm("{\n\t.reg .b16 lo, hi;\n\t"

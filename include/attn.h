@@ -31,6 +31,8 @@
 #ifndef ATTN_FWD_GB300_ATTN_H
 #define ATTN_FWD_GB300_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -210,6 +212,49 @@ int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size,
  * normal operation.  Process-wide, not thread-safe; attn_fwd_noalloc ignores it.
  */
 int attn_debug_inject(int mode);
+
+/*
+ * attn_bwd -- enqueue the backward of attn_fwd on `stream`: the gradients of
+ * sum(dout * O) with respect to q, k and v, for the same mask, block size and
+ * sm_scale, from the forward's o and lse (the "Fused Attention" page saves
+ * exactly these for a backward it does not define; the gradients follow from
+ * the definition above by the chain rule through the softmax):
+ *
+ *     P  = exp(sm_scale Q K^T - lse)  (0 outside the mask),  Di = dout_i . o_i
+ *     dv = P^T dout,   dS = P * (dout v^T - Di),
+ *     dq = sm_scale dS k,   dk = sm_scale dS^T q
+ *
+ *   q, k, v, o, dout  [B, H, L, D] of `dtype`, device memory, read only
+ *                     (o and lse as attn_fwd wrote them).
+ *   lse               [B, H, L] fp32, device memory, read only.
+ *   dq, dk, dv        outputs, [B, H, L, D] of `dtype`, device memory, fully
+ *                     written (no accumulation into them; no atomics, so the
+ *                     results are deterministic).
+ *   workspace         device scratch of at least attn_bwd_workspace_size(B, H,
+ *                     L) bytes, 16-byte aligned, owned by the caller, free for
+ *                     reuse once the call's work on `stream` has completed.
+ *   D                 a multiple of 8 from 8 to 128 (kernels for 64 and 128);
+ *                     other arguments as for attn_fwd.
+ *
+ * Three kernels run in order on `stream`.  Returns ATTN_OK once enqueued;
+ * ATTN_ERR_ARG if workspace_bytes is too small or sm_scale is not finite;
+ * argument errors as attn_fwd, all before any CUDA call; device-side
+ * timeouts are reported through attn_last_device_status.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, void *workspace,
+             size_t workspace_bytes, int B, int H, int L, int D, int mask_kind,
+             int block_size, float sm_scale, int dtype, void *stream);
+
+/* Bytes of workspace attn_bwd needs: two fp32 values per row, rows padded to
+ * whole 128-row tiles per head (0 for negative sizes). */
+size_t attn_bwd_workspace_size(int B, int H, int L);
+
+/* Algorithmic work of one attn_bwd: flops = 2.5 x the forward's (five
+ * products of its size: S, dP, dV, dK, dQ), bytes = q, k, v, o, dout read and
+ * dq, dk, dv written once, plus lse; returns an attn_status. */
+int attn_bwd_work(int B, int H, int L, int D, int mask_kind, int block_size, int dtype,
+                  double *flops, double *bytes);
 
 /* ABI version of this header: (major << 16) | minor. */
 int attn_abi_version(void);

@@ -1,0 +1,122 @@
+"""GPU parity of the backward (``attn_bwd``) against the oracle's gradients of
+the attention definition.
+
+The forward runs on the GPU (its o and lse feed the backward, as in use); the
+oracle computes dQ, dK, dV in fp64 from q, k, v and dO alone.  Tolerance, per
+element, from the arithmetic of the GPU path: P and dS are rounded to the
+16-bit type before their products, Di comes from the 16-bit O, and the results
+are rounded once more, so
+
+    |GPU - oracle| <= 2 u (b + |oracle|) + 1e-6
+
+with u the unit roundoff of the type (2^-11 fp16, 2^-8 bf16) and b the
+oracle's magnitude bound of each element (``oracle.attention_bwd(...,
+bounds=True)``); the factor 2 covers the fp32 accumulations.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_inputs import BLOCK_DIAG, CAUSAL, DENSE, make_qkv, make_qkv_far_below_zero
+
+pytestmark = pytest.mark.gpu
+
+U = {torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+
+
+@pytest.fixture(scope="module")
+def af():
+    import attention_forward_15_gb300 as m
+    from attention_forward_15_gb300 import _build_ext
+    _build_ext.build()
+    m.load_library()
+    assert torch.cuda.is_available()
+    return m
+
+
+def _dout(q, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(q.shape, generator=g).to(q.dtype)
+
+
+def _case(af, B, H, L, D, mask, bs, dt, scale=None, seed=42, qkv=None):
+    q, k, v = make_qkv(B, H, L, D, dt, seed=seed) if qkv is None else qkv
+    g = _dout(q, seed + 1)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    o, lse = af.fwd(qd, kd, vd, mask, bs, scale)
+    dq, dk, dv = af.bwd(qd, kd, vd, o, lse, gd, mask, bs, scale)
+    torch.cuda.synchronize()
+    st, det = af.last_device_status(0)
+    assert st == 0, f"device status {st} ({det:#x})"
+    ref = oracle.attention_bwd(q, k, v, g, mask, bs, float(np.float32(scale)), bounds=True)
+    u = U[dt]
+    for name, got, want, b in (("dq", dq, ref[0], ref[3]), ("dk", dk, ref[1], ref[4]),
+                               ("dv", dv, ref[2], ref[5])):
+        gg = got.double().cpu().numpy()
+        assert np.isfinite(gg).all(), f"{name}: non-finite"
+        err = np.abs(gg - want)
+        tol = 2.0 * u * (b + np.abs(want)) + 1e-6
+        worst = np.unravel_index(np.argmax(err - tol), err.shape)
+        assert (err <= tol).all(), (f"{name}: max(err - tol) = {(err - tol).max():.3e} at {worst} "
+                                    f"(err {err[worst]:.3e}, tol {tol[worst]:.3e}, ref {want[worst]:.3e})")
+
+
+CASES = [
+    # (B, H, L, D, mask, bs, dtype)
+    (1, 2, 256, 64, DENSE, 0, torch.float16),
+    (2, 2, 384, 64, CAUSAL, 0, torch.bfloat16),
+    (1, 2, 512, 64, BLOCK_DIAG, 64, torch.float16),
+    (1, 3, 300, 64, DENSE, 0, torch.bfloat16),          # ragged tail
+    (1, 2, 256, 128, DENSE, 0, torch.bfloat16),
+    (1, 2, 640, 128, CAUSAL, 0, torch.float16),
+    (1, 2, 512, 128, BLOCK_DIAG, 256, torch.bfloat16),
+    (1, 2, 333, 128, CAUSAL, 0, torch.float16),         # ragged causal
+    (1, 2, 512, 64, BLOCK_DIAG, 16, torch.bfloat16),
+    (1, 2, 256, 32, CAUSAL, 0, torch.float16),          # padded head dims
+    (1, 2, 256, 96, DENSE, 0, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}H{}L{}D{}m{}bs{}{}".format(
+    *c[:6], "f16" if c[6] == torch.float16 else "bf16"))
+def test_bwd_all_elements(af, case):
+    _case(af, *case)
+
+
+@pytest.mark.parametrize("sign", [1, -1])
+def test_bwd_scores_far_below_zero(af, sign):
+    """Every score near -200 and a ragged tail: P comes from lse, and keys past
+    L (zero rows) are cut before their p can overflow."""
+    q, k, v, scale = make_qkv_far_below_zero(1, 2, 333, 64, torch.float16, sign)
+    _case(af, 1, 2, 333, 64, DENSE, 0, torch.float16, scale=scale, qkv=(q, k, v))
+
+
+def test_bwd_deterministic(af):
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in make_qkv(1, 4, 512, 128, torch.bfloat16, seed=3))
+    g = _dout(q.cpu(), 4).to(dev)
+    o, lse = af.fwd(q, k, v, CAUSAL)
+    a = af.bwd(q, k, v, o, lse, g, CAUSAL)
+    b = af.bwd(q, k, v, o, lse, g, CAUSAL)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_bwd_argument_errors(af):
+    dev = torch.device("cuda", 0)
+    q = torch.zeros((1, 1, 128, 256), dtype=torch.float16, device=dev)
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
+    with pytest.raises(af.AttnError) as e:
+        af.bwd(q, q, q, q, lse, q)                    # D = 256 has no backward kernel
+    assert e.value.status == 4
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.float16, device=dev)
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
+    with pytest.raises(af.AttnError) as e:
+        af.bwd(q, q, q, q, lse, q, workspace=torch.empty(16, dtype=torch.uint8, device=dev))
+    assert e.value.status == 8
