@@ -602,15 +602,15 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     prm.bs = mask_kind == ATTN_MASK_BLOCK_DIAG ? block_size : 0;
     prm.n_t = (L + 127) / 128;
     prm.n_pad = prm.n_t * 128;
-    prm.lse2 = static_cast<float *>(workspace);
-    prm.delta = prm.lse2 + static_cast<size_t>(bh) * prm.n_pad;
+    prm.nlse2 = static_cast<float *>(workspace);
+    prm.ndelta = prm.nlse2 + static_cast<size_t>(bh) * prm.n_pad;
     prm.scale = sm_scale;
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
     prm.d_out = D;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == ATTN_BF16;
-    // Di, lse * log2(e), padded per head
+    // -Di and -lse * log2(e), padded per head
     {
         const long long rows = bh * prm.n_pad;
         long long blocks = (rows + 31) / 32;

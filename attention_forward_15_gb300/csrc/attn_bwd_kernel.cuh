@@ -11,14 +11,14 @@
 //   dQ_i = sm_scale sum_j dS_ij k_j     dK_j = sm_scale sum_i dS_ij q_i
 //
 // Three kernels, no atomics (results are deterministic):
-//   * attn_bwd_prep_kernel: Di per row, and per-head copies of lse*log2(e) and
-//     Di padded to whole 128-row tiles (padding rows: +inf and 0, so that rows
-//     past L give P = 0 wherever they are read);
+//   * attn_bwd_prep_kernel: Di per row, and per-head copies of -lse*log2(e)
+//     and -Di padded to whole 128-row tiles (padding rows: -inf and 0, so that
+//     rows past L give P = 0 wherever they are read);
 //   * attn_bwd_kernel<D, BF16, false> ("dK/dV"): one CTA per (head, key tile);
 //     K and V of the tile stay in shared memory while the query tiles that
 //     attend it stream through a ring; per query tile
 //         S^T = K Q^T, dP^T = V dO^T       (tcgen05, fp32 in tensor memory)
-//         P^T, dS^T in the compute warps   (one thread per key row)
+//         P^T, dS^T in the compute warps   (one thread per key row and half)
 //         dV += P^T dO, dK += dS^T Q       (A operand from tensor memory)
 //   * attn_bwd_kernel<D, BF16, true> ("dQ"): one CTA per (head, query tile);
 //     Q and dO stay while the attended key tiles stream; per key tile
@@ -28,11 +28,14 @@
 // streams pairs (R0, R1); the products are S = F0 R0^T and dP = F1 R1^T in
 // either kernel, then (dK/dV) ACC0 += P R1 and, in both, ACC1 += dS R0.
 //
-// Tensor memory (512 columns): S at 0, dP at 128, ACC0 at 256, ACC1 at 256 + D.
-// P (16-bit pairs) is written over the first 64 columns of S and dS over the
-// first 64 of dP, as the columns are consumed; the next tile's S and dP are
-// issued after the products that read them, on the same in-order MMA pipe.
-// D is 64 or 128 (S, dP and two D-wide accumulators fill the 512 columns).
+// Each streamed tile is taken as two halves of 64 rows, each with S and dP
+// buffers of its own in tensor memory, so the MMA pipe computes one half's
+// products while the compute warps work on the other:
+//   S_0 | dP_0 | S_1 | dP_1 (64 columns each) | ACC0 (D) | ACC1 (D).
+// P (16-bit pairs) is written over the first 32 columns of its S and dS over
+// the first 32 of its dP, as the columns are consumed; a half's next S and dP
+// are issued after the products that read its P and dS, on the same in-order
+// MMA pipe.  D is 64 or 128 (256 + 2D columns).
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -43,8 +46,8 @@ struct BwdParams {
     const void *o;           // prep: forward output [BH, L, d_out] 16-bit
     const void *dout;        // prep: output gradient [BH, L, d_out] 16-bit
     const float *lse;        // prep: forward lse [BH, L] (natural log)
-    float *lse2;             // [BH, n_pad]: lse * log2(e), +inf past L
-    float *delta;            // [BH, n_pad]: Di, 0 past L
+    float *nlse2;            // [BH, n_pad]: -lse * log2(e), -inf past L
+    float *ndelta;           // [BH, n_pad]: -Di, 0 past L
     void *g0;                // dK/dV: dK, dQ: dQ   [BH, L, d_out] 16-bit
     void *g1;                // dK/dV: dV           [BH, L, d_out] 16-bit
     unsigned int *status;
@@ -58,9 +61,11 @@ struct BwdParams {
 
 // ------------------------------------------------------------------ prep
 
-// Di = sum_d dO[i,d] O[i,d] (fp32) and lse2 = lse * log2(e) for every row of
-// every head, padded to n_pad rows.  Eight threads per row, 16 bytes each per
-// step, reduced by shuffles; grid-stride over rows.
+// Di = sum_d dO[i,d] O[i,d] (fp32) for every row of every head, stored as -Di
+// with -lse * log2(e) beside it (negated so that the tile kernels take them
+// with one packed fma and one packed add), padded to n_pad rows.  Eight
+// threads per row, 16 bytes each per step, reduced by shuffles; grid-stride
+// over rows.
 template <bool BF16>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
     griddep_wait();
@@ -92,8 +97,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
         if (sub == 0) {
-            p.delta[r] = i < p.L ? acc : 0.f;
-            p.lse2[r] = i < p.L ? p.lse[static_cast<size_t>(bh) * p.L + i] * 1.4426950408889634f : INFINITY;
+            p.ndelta[r] = i < p.L ? -acc : 0.f;
+            p.nlse2[r] = i < p.L ? p.lse[static_cast<size_t>(bh) * p.L + i] * -1.4426950408889634f : -INFINITY;
         }
     }
 }
@@ -106,19 +111,24 @@ struct BwdCfg {
     static constexpr int CHUNK_BYTES = 128 * 128;
     static constexpr int TILE_BYTES = 128 * D * 2;
     static constexpr int NS = D == 64 ? 3 : 2;          // ring stages of streamed pairs
-    static constexpr int THREADS = 192;                 // 4 compute warps, TMA warp, MMA warp
-    static constexpr int WARP_TMA = 4, WARP_MMA = 5;
-    static constexpr int VEC_BYTES = DQ ? 0 : 2 * 128 * 4;   // lse2 and Di of one query tile
+    // two compute warpgroups (warps 0-3 take the first 64-row half of every
+    // streamed tile, warps 4-7 the second), a TMA warp and an MMA warp
+    static constexpr int THREADS = 320;
+    static constexpr int WARP_TMA = 8, WARP_MMA = 9;
+    static constexpr int VEC_BYTES = DQ ? 0 : 2 * 128 * 4;   // -lse2 and -Di of one query tile
     static constexpr int OFF_FIX = 0;                        // F0 | F1
     static constexpr int OFF_RING = 2 * TILE_BYTES;          // NS x (R0 | R1)
     static constexpr int OFF_VEC = OFF_RING + NS * 2 * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_VEC + NS * VEC_BYTES;
-    static constexpr int B_FIX = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_SFULL = 1 + 2 * NS;
-    static constexpr int B_PFULL = B_SFULL + 1, B_DONE = B_PFULL + 1, B_DRAIN = B_DONE + 1;
+    static constexpr int B_FIX = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_SFULL = 1 + 2 * NS;   // SFULL, PFULL: one per half
+    static constexpr int B_PFULL = B_SFULL + 2, B_DONE = B_PFULL + 2, B_DRAIN = B_DONE + 1;
     static constexpr int NBAR = B_DRAIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // [0]: TMEM base, [1]: abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC0 = 256, COL_ACC1 = 256 + D;
+    static constexpr int HALF_BYTES = 64 * 128;          // 64 rows of a 128-byte-wide box
+    __device__ static constexpr uint32_t col_s(int h) { return 128u * static_cast<uint32_t>(h); }
+    __device__ static constexpr uint32_t col_dp(int h) { return 128u * static_cast<uint32_t>(h) + 64u; }
+    static constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = 256 + D;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(D == 64 || D == 128, "backward head dim");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -146,37 +156,51 @@ __device__ __forceinline__ void bwd_range(const BwdParams &p, bool dq, int f, in
 }
 
 // dS (and P) of one 32-column chunk: rows are this thread's TMEM lane, columns
-// c0..c0+31 of the tile.  S, dP: fp32 raw scores and dP of the chunk.
-// Column-indexed (dK/dV) or row (dQ) lse2 / Di; `keep` masks (row, column).
+// c0..c0+31 of the tile.  S, dP: fp32 raw scores and dP of the chunk.  The
+// negated lse2 and Di come per row (dQ: nl_row, nd_row) or per column (dK/dV:
+// the shared-memory vectors, read four at a time); packed fp32x2 arithmetic as
+// in the forward; `keep` masks (row, column).
 template <bool BF16, bool DQ, bool MASKED>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&S)[32], const uint32_t (&dP)[32], float sc,
-                                          float row_lse2, float row_delta, const float *col_lse2,
-                                          const float *col_delta, int c0, int mask, int bs, int L,
+                                          float nl_row, float nd_row, const float *col_nl,
+                                          const float *col_nd, int c0, int mask, int bs, int L,
                                           int row_idx, int col_base, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+    const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-        float pv[2], dv[2];
+        float2 nl, nd;
+        if constexpr (DQ) {
+            nl = make_float2(nl_row, nl_row);
+            nd = make_float2(nd_row, nd_row);
+        } else {
+            const float4 a = reinterpret_cast<const float4 *>(col_nl + c0)[e >> 1];
+            const float4 b = reinterpret_cast<const float4 *>(col_nd + c0)[e >> 1];
+            nl = (e & 1) ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
+            nd = (e & 1) ? make_float2(b.z, b.w) : make_float2(b.x, b.y);
+        }
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(S[2 * e]), __uint_as_float(S[2 * e + 1])), sc2, nl);
+        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if constexpr (MASKED) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = c0 + 2 * e + h;
-            const float l2 = DQ ? row_lse2 : col_lse2[c];
-            const float dl = DQ ? row_delta : col_delta[c];
-            float pp = ex2_approx(fmaf(__uint_as_float(S[2 * e + h]), sc, -l2));
-            if constexpr (MASKED) {
+            for (int h = 0; h < 2; ++h) {
                 // (query, key) of this element; keys past L are zero rows whose
                 // p could overflow when lse is very negative, so they are cut too
+                const int c = c0 + 2 * e + h;
                 const int qi = DQ ? row_idx : col_base + c;
                 const int kj = DQ ? col_base + c : row_idx;
                 bool keep = kj < L;
                 if (mask == kMaskCausal) keep = keep && kj <= qi;
                 else if (mask == kMaskBlock) keep = keep && (kj / bs) == (qi / bs);
-                if (!keep) pp = 0.f;
+                if (!keep) {
+                    if (h == 0) pp.x = 0.f;
+                    else pp.y = 0.f;
+                }
             }
-            pv[h] = pp;
-            dv[h] = pp * (__uint_as_float(dP[2 * e + h]) - dl);
         }
-        pk[e] = pack2<BF16>(pv[0], pv[1]);
-        dk[e] = pack2<BF16>(dv[0], dv[1]);
+        const float2 ds = __fmul2_rn(
+            pp, __fadd2_rn(make_float2(__uint_as_float(dP[2 * e]), __uint_as_float(dP[2 * e + 1])), nd));
+        pk[e] = pack2<BF16>(pp.x, pp.y);
+        dk[e] = pack2<BF16>(ds.x, ds.y);
     }
 }
 
@@ -211,8 +235,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             mbar_init(bar(C::B_FULL + s), 1);
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
-        mbar_init(bar(C::B_SFULL), 1);
-        mbar_init(bar(C::B_PFULL), 4);       // one arrival per compute warp
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(C::B_SFULL + h), 1);
+            mbar_init(bar(C::B_PFULL + h), 4);   // one arrival per warp of half h's group
+        }
         mbar_init(bar(C::B_DONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         misc[1] = 0;
@@ -272,8 +298,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             if constexpr (!DQ) {
                 const size_t off = static_cast<size_t>(bh) * p.n_pad + static_cast<size_t>(j) * 128;
                 const uint32_t vdst = s_base + C::OFF_VEC + s * C::VEC_BYTES;
-                bulk_load_1d(vdst, p.lse2 + off, 512, bar(C::B_FULL + s));
-                bulk_load_1d(vdst + 512, p.delta + off, 512, bar(C::B_FULL + s));
+                bulk_load_1d(vdst, p.nlse2 + off, 512, bar(C::B_FULL + s));
+                bulk_load_1d(vdst + 512, p.ndelta + off, 512, bar(C::B_FULL + s));
             }
             ++issued;
         }
@@ -287,11 +313,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
         // ================================================================ MMA issuer
-        constexpr uint32_t IDESC_SS = idesc_f16_f32acc(BF16, 128, 128, false);
+        constexpr uint32_t IDESC_SS = idesc_f16_f32acc(BF16, 128, 64, false);
         constexpr uint32_t IDESC_ACC = idesc_f16_f32acc(BF16, 128, D, true);
         const uint32_t f0 = s_base + C::OFF_FIX, f1 = f0 + C::TILE_BYTES;
-        // X = A B^T over the head dim: both K-major, k-step kk = head-dim
-        // columns [16kk, 16kk+16): box kk/4, 32-byte offset kk%4.
+        // X = A B^T over the head dim for 64 rows of B: both K-major, k-step kk
+        // = head-dim columns [16kk, 16kk+16): box kk/4, 32-byte offset kk%4.
         auto issue_ss = [&](uint32_t a, uint32_t b, uint32_t dcol) {
             const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
@@ -300,43 +326,52 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
                 mma_ss(tmem + dcol, ad + off, bd + off, IDESC_SS, kk > 0 ? 1u : 0u);
             }
         };
-        // ACC += A(TMEM, 16-bit pairs) B, B MN-major: k-step kk = rows
-        // [16kk, 16kk+16) of B; its 64-column boxes are CHUNK_BYTES apart.
+        // ACC += A(TMEM, 16-bit pairs) B over 64 rows of B, B MN-major: k-step kk
+        // = rows [16kk, 16kk+16); its 64-column boxes are CHUNK_BYTES apart.
         auto issue_acc = [&](uint32_t acol, uint32_t b, uint32_t dcol, bool accumulate) {
             const uint64_t bd = sdesc_sw128(b, C::CHUNK_BYTES, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 128 / 16; ++kk)
+            for (int kk = 0; kk < 64 / 16; ++kk)
                 mma_ts(tmem + dcol, tmem + acol + kk * 8, bd + static_cast<uint64_t>(kk * 128), IDESC_ACC,
                        (accumulate || kk > 0) ? 1u : 0u);
+        };
+        // S_h and dP_h of the tile in ring stage `stage`
+        auto issue_half = [&](int stage, int h) {
+            const uint32_t r0 = s_base + C::OFF_RING + stage * 2 * C::TILE_BYTES + h * C::HALF_BYTES;
+            issue_ss(f0, r0, C::col_s(h));
+            issue_ss(f1, r0 + C::TILE_BYTES, C::col_dp(h));
+            mma_commit(bar(C::B_SFULL + h));
         };
         bool ok = nn > 0;
         if (ok) ok = wait_warp(bar(C::B_FIX), 0, kSiteQFull);
         if (ok) ok = wait_warp(bar(C::B_FULL + 0), 0, kSiteKvFullK);
         if (ok) {
             tc_fence_after();
-            const uint32_t r = s_base + C::OFF_RING;
-            issue_ss(f0, r, C::COL_S);
-            issue_ss(f1, r + C::TILE_BYTES, C::COL_DP);
-            mma_commit(bar(C::B_SFULL));
+            issue_half(0, 0);
+            issue_half(0, 1);
         }
         for (int t = 0; t < nn && ok; ++t) {
             const int s = t % C::NS;
-            ok = wait_warp(bar(C::B_PFULL), t & 1, kSitePFull);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t r0 = s_base + C::OFF_RING + s * 2 * C::TILE_BYTES, r1 = r0 + C::TILE_BYTES;
-            if constexpr (!DQ) issue_acc(C::COL_S, r1, C::COL_ACC0, t > 0);     // dV += P^T dO
-            issue_acc(C::COL_DP, r0, C::COL_ACC1, t > 0);                        // dK += dS^T Q | dQ += dS K
-            mma_commit(bar(C::B_EMPTY + s));
-            if (t + 1 < nn) {
-                const int s2 = (t + 1) % C::NS;
-                ok = wait_warp(bar(C::B_FULL + s2), ((t + 1) / C::NS) & 1, kSiteKvFullK);
+            const int s2 = (t + 1) % C::NS;
+#pragma unroll 1
+            for (int h = 0; h < 2 && ok; ++h) {
+                ok = wait_warp(bar(C::B_PFULL + h), t & 1, kSitePFull);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t q0 = s_base + C::OFF_RING + s2 * 2 * C::TILE_BYTES;
-                issue_ss(f0, q0, C::COL_S);
-                issue_ss(f1, q0 + C::TILE_BYTES, C::COL_DP);
-                mma_commit(bar(C::B_SFULL));
+                const uint32_t r0 = s_base + C::OFF_RING + s * 2 * C::TILE_BYTES + h * C::HALF_BYTES;
+                const uint32_t r1 = r0 + C::TILE_BYTES;
+                const bool acc = t > 0 || h > 0;
+                if constexpr (!DQ) issue_acc(C::col_s(h), r1, C::COL_ACC0, acc);   // dV += P^T dO
+                issue_acc(C::col_dp(h), r0, C::COL_ACC1, acc);                       // dK += dS^T Q | dQ += dS K
+                if (h == 1) mma_commit(bar(C::B_EMPTY + s));
+                if (t + 1 < nn) {
+                    if (h == 0) {
+                        ok = wait_warp(bar(C::B_FULL + s2), ((t + 1) / C::NS) & 1, kSiteKvFullK);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    issue_half(s2, h);
+                }
             }
         }
         if (ok && nn > 0) mma_commit(bar(C::B_DONE));
@@ -347,75 +382,83 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         __syncwarp();
     } else {
         // ================================================================ compute warps
-        const int row = warp * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        // warpgroup h takes half h (rows 64h..64h+63 of every streamed tile);
+        // each thread owns one TMEM lane, i.e. one row of the fixed tile
+        const int h = warp >> 2;
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int row_idx = f * 128 + row;                 // query (dQ) or key (dK/dV) index
         const float sc = p.scale_log2;
-        float row_lse2 = 0.f, row_delta = 0.f;
+        float row_nl = 0.f, row_nd = 0.f;
         if constexpr (DQ) {
-            row_lse2 = p.lse2[static_cast<size_t>(bh) * p.n_pad + row_idx];
-            row_delta = p.delta[static_cast<size_t>(bh) * p.n_pad + row_idx];
+            row_nl = p.nlse2[static_cast<size_t>(bh) * p.n_pad + row_idx];
+            row_nd = p.ndelta[static_cast<size_t>(bh) * p.n_pad + row_idx];
         }
         bool ok = true;
         for (int t = 0; t < nn && ok; ++t) {
-            ok = wait_warp(bar(C::B_SFULL), t & 1, kSiteSFull);
-            if (!ok) break;
-            tc_fence_after();
             const int s = t % C::NS;
             const int j = lo + t;
             const float *vec = reinterpret_cast<const float *>(smem + C::OFF_VEC + s * C::VEC_BYTES);
             // tiles that cross the mask, and (dQ) a ragged last key tile
             const bool masked = (p.mask == kMaskCausal && j == f) || (p.mask == kMaskBlock && (p.bs % 128) != 0) ||
                                 (DQ && (j + 1) * 128 > p.L);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(tmem + lane_off + C::COL_S + 32 * c, sv);
-                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * c, dpv);
-                tmem_wait_ld();
+            ok = wait_warp(bar(C::B_SFULL + h), t & 1, kSiteSFull);
+            if (!ok) break;
+            tc_fence_after();
+            // the half's S and dP in one round trip
+            uint32_t sv[64], dpv[64];
+            tmem_ld32(tmem + lane_off + C::col_s(h), *reinterpret_cast<uint32_t(*)[32]>(sv));
+            tmem_ld32(tmem + lane_off + C::col_s(h) + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            tmem_ld32(tmem + lane_off + C::col_dp(h), *reinterpret_cast<uint32_t(*)[32]>(dpv));
+            tmem_ld32(tmem + lane_off + C::col_dp(h) + 32, *reinterpret_cast<uint32_t(*)[32]>(dpv + 32));
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16], dk[16];
+                const int c0 = 64 * h + 32 * c;     // column of the chunk in the tile
+                const uint32_t(&sc32)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + 32 * c);
+                const uint32_t(&dp32)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dpv + 32 * c);
                 if (masked)
-                    bwd_chunk<BF16, DQ, true>(sv, dpv, sc, row_lse2, row_delta, vec, vec + 128, 32 * c, p.mask,
-                                              p.bs, p.L, row_idx, j * 128, pk, dk);
+                    bwd_chunk<BF16, DQ, true>(sc32, dp32, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
+                                              p.L, row_idx, j * 128, pk, dk);
                 else
-                    bwd_chunk<BF16, DQ, false>(sv, dpv, sc, row_lse2, row_delta, vec, vec + 128, 32 * c, p.mask,
-                                               p.bs, p.L, row_idx, j * 128, pk, dk);
-                // columns [16c, 16c+16) of S and dP were read in this or an earlier chunk
-                if constexpr (!DQ) tmem_st16(tmem + lane_off + C::COL_S + 16 * c, pk);
-                tmem_st16(tmem + lane_off + C::COL_DP + 16 * c, dk);
+                    bwd_chunk<BF16, DQ, false>(sc32, dp32, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
+                                               p.L, row_idx, j * 128, pk, dk);
+                // the whole half is in registers, so its columns may be overwritten
+                if constexpr (!DQ) tmem_st16(tmem + lane_off + C::col_s(h) + 16 * c, pk);
+                tmem_st16(tmem + lane_off + C::col_dp(h) + 16 * c, dk);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_PFULL));
+            if (lane == 0) mbar_arrive(bar(C::B_PFULL + h));
         }
         if (ok && nn > 0) ok = wait_warp(bar(C::B_DONE), 0, kSiteODone);
         if (ok && nn > 0) {
             tc_fence_after();
             const bool row_valid = row_idx < p.L;
-            // ACC1 (dK or dQ, times sm_scale) to g0; dK/dV: ACC0 (dV) to g1
+            // dK/dV: group 0 writes ACC1 (dK, times sm_scale) to g0, group 1 ACC0
+            // (dV) to g1; dQ: the groups split ACC1 (times sm_scale) by 32-column chunks
+            const bool to_g0 = DQ || h == 0;
+            const uint32_t acol = to_g0 ? C::COL_ACC1 : C::COL_ACC0;
+            const float mul = to_g0 ? p.scale : 1.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(to_g0 ? p.g0 : p.g1) +
+                                                   ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out) * 2);
 #pragma unroll 1
-            for (int which = 0; which < (DQ ? 1 : 2); ++which) {
-                const uint32_t acol = which == 0 ? C::COL_ACC1 : C::COL_ACC0;
-                const float mul = which == 0 ? p.scale : 1.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(which == 0 ? p.g0 : p.g1) +
-                                                       ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out) * 2);
-#pragma unroll 1
-                for (int c = 0; c < D / 32 && 32 * c < p.d_out; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(tmem + lane_off + acol + 32 * c, raw);
-                    tmem_wait_ld();
-                    uint32_t w16[16];
+            for (int c = DQ ? h : 0; c < D / 32 && 32 * c < p.d_out; c += DQ ? 2 : 1) {
+                uint32_t raw[32];
+                tmem_ld32(tmem + lane_off + acol + 32 * c, raw);
+                tmem_wait_ld();
+                uint32_t w16[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * mul, __uint_as_float(raw[2 * e + 1]) * mul);
-                    if (row_valid) {
+                for (int e = 0; e < 16; ++e)
+                    w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * mul, __uint_as_float(raw[2 * e + 1]) * mul);
+                if (row_valid) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            if (32 * c + 8 * v4 < p.d_out)
-                                dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
-                                                             w16[4 * v4 + 3]);
-                    }
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        if (32 * c + 8 * v4 < p.d_out)
+                            dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
+                                                         w16[4 * v4 + 3]);
                 }
             }
         }

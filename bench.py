@@ -248,6 +248,50 @@ def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None
     return ms, {"rotating_sets": nsets, "set_bytes": per_set, "graph_launches": chunk}
 
 
+def time_bwd(af, w, dev, steps, warmup):
+    """Device time per step (ms) of the backward on workload w: o and lse from
+    one forward per input set, dout drawn like the inputs; sets rotate past L2
+    and the steps replay from a CUDA graph (three kernels per step)."""
+    q, k, v = make_device_inputs(w, dev)
+    per_set = 8 * q.numel() * q.element_size()
+    nsets = rotation_sets(w, dev, per_set)
+    lib = af.load_library()
+    sets = []
+    for s in range(nsets):
+        qs, ks, vs = (q, k, v) if s == 0 else (q.clone(), k.clone(), v.clone())
+        g = torch.randn(q.shape, device=dev).to(q.dtype)
+        o, lse = af.fwd(qs, ks, vs, w.mask, w.block_size, w.sm_scale)
+        ws = torch.empty(max(16, lib.attn_bwd_workspace_size(w.B, w.H, w.L)), dtype=torch.uint8, device=dev)
+        sets.append((qs, ks, vs, o, lse, g, torch.empty_like(q), torch.empty_like(q), torch.empty_like(q), ws))
+
+    def step(i):
+        qs, ks, vs, o, lse, g, dq, dk, dv, ws = sets[i % nsets]
+        af.bwd(qs, ks, vs, o, lse, g, w.mask, w.block_size, w.sm_scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for i in range(max(warmup, 1)):
+            step(i)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(steps):
+            step(i)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    st, det = af.last_device_status(dev.index)
+    if st != 0:
+        raise RuntimeError(f"device status {st} (detail {det:#x}) after the backward")
+    return e0.elapsed_time(e1) / steps
+
+
 def time_e2e(af, w, dev, steps, warmup):
     """End to end through the public host API: each step copies q, k, v from
     pinned host memory, runs the forward and copies o and lse back."""
@@ -415,6 +459,17 @@ def main():
             fp8_pv[name] = {"mask": MASK_NAMES[ow.mask], "ms": round(ms2, 4),
                             "tflops": round(f2 / (ms2 * 1e-3) / 1e12, 2),
                             "frac_of_bf16_peak": round(f2 / (ms2 * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    # The backward (attn_bwd: dQ, dK, dV) on the D <= 128 workloads.
+    bwd_lines = {}
+    if not args.no_all:
+        for name in (w.name, "causal_b2h32l4096d128_bf16"):
+            ow = WORKLOADS[name]
+            fb, _ = af.bwd_work(ow.B, ow.H, ow.L, ow.D, ow.mask, ow.block_size, ow.dtype)
+            msb = time_bwd(af, ow, dev, 40 if ow.L >= 4096 else 100, 3)
+            bwd_lines[name] = {"mask": MASK_NAMES[ow.mask], "ms": round(msb, 4),
+                               "tflops": round(fb / (msb * 1e-3) / 1e12, 2),
+                               "frac_of_bf16_peak": round(fb / (msb * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                               "flops": "2.5 x the forward's (S, dP, dV, dK, dQ)"}
     if dist:
         dist.barrier()
     if rank != 0:
@@ -446,6 +501,7 @@ def main():
         "clocks": clocks,
         "per_workload": per_mask or None,
         "fp8_pv_variant": fp8_pv or None,
+        "backward": bwd_lines or None,
     }
     out["cpu_baseline"] = None if args.lean else cpu_baseline(w)
     print(json.dumps(out), flush=True)
