@@ -52,6 +52,9 @@ def parse_args():
                     help="skip the per-mask-kind measurements of the other workloads")
     ap.add_argument("--soak-s", type=float, default=2.0,
                     help="seconds of untimed launches before the timed region (clock sampling)")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="time only the backward (attn_bwd) on --workload and print one line "
+                         "(for profiler runs)")
     ap.add_argument("--lean", action="store_true",
                     help="only the device-timed line: no soak, e2e, CPU baseline or other "
                          "workloads (for profiler runs)")
@@ -419,6 +422,17 @@ def main():
         dist = tdist
 
     peaks, peaks_kind = load_peaks()
+    if args.bwd_only:
+        fb, _ = af.bwd_work(w.B, w.H, w.L, w.D, w.mask, w.block_size, w.dtype)
+        msb = reduce_max(time_bwd(af, w, dev, args.steps, args.warmup), dist, dev)
+        if rank == 0:
+            print(json.dumps({"metric": "attention bwd TFLOP/s (2.5 x forward flops)", "workload": w.name,
+                              "value": round(fb * world / (msb * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                              "ms_per_step": round(msb, 5), "steps": args.steps, "warmup": args.warmup}),
+                  flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
     flops, nbytes = af.work(w.B, w.H, w.L, w.D, w.mask, w.block_size, w.dtype)
     if args.lean:
         args.soak_s, args.no_all = 0.0, True
