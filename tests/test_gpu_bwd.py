@@ -120,3 +120,31 @@ def test_bwd_argument_errors(af):
     with pytest.raises(af.AttnError) as e:
         af.bwd(q, q, q, q, lse, q, workspace=torch.empty(16, dtype=torch.uint8, device=dev))
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("name", ["causal_b2h32l4096d128_bf16", "dense_b4h16l1024d64_f16"])
+def test_bwd_full_size_heads(af, name):
+    """The backward of a full-size workload, in one launch sequence as the
+    benchmark runs it; the first and the last head compared element by element
+    with the oracle's gradients of those heads."""
+    from attn_inputs import WORKLOADS
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w.B, w.H, w.L, w.D, w.dtype, seed=w.seed)
+    g = _dout(q, 99)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    o, lse = af.fwd(qd, kd, vd, w.mask, w.block_size, w.sm_scale)
+    grads = af.bwd(qd, kd, vd, o, lse, gd, w.mask, w.block_size, w.sm_scale)
+    torch.cuda.synchronize()
+    assert af.last_device_status(0)[0] == 0
+    u = U[w.dtype]
+    # the two heads side by side, so that the oracle runs them in parallel
+    pick = lambda t: torch.cat([t[0:1, 0:1], t[w.B - 1:w.B, w.H - 1:w.H]], dim=1)
+    ref = oracle.attention_bwd(pick(q), pick(k), pick(v), pick(g), w.mask, w.block_size,
+                               float(np.float32(w.sm_scale)), bounds=True)
+    for name_, got, want, bnd in zip(("dq", "dk", "dv"), grads, ref[:3], ref[3:]):
+        gg = pick(got.cpu()).double().numpy()
+        err = np.abs(gg - want)
+        tol = 2.0 * u * (bnd + np.abs(want)) + 1e-6
+        assert np.isfinite(gg).all() and (err <= tol).all(), \
+            f"{name_}: max(err - tol) = {(err - tol).max():.3e}"

@@ -243,6 +243,21 @@ def test_host_buffer_entry_point(af, mask, bs, dt):
     assert e.value.status == 4
 
 
+@pytest.mark.parametrize("B,H,L,D,mask,dt", [(4, 16, 1024, 64, DENSE, torch.float16),
+                                             (3, 5, 1000, 128, CAUSAL, torch.bfloat16)])
+def test_host_entry_point_large(af, B, H, L, D, mask, dt):
+    """attn_fwd_host on the headline size and on a ragged causal D = 128 case:
+    the same bytes as attn_fwd on device buffers."""
+    q, k, v = (t.pin_memory() for t in make_qkv(B, H, L, D, dt, seed=8))
+    dev = torch.device("cuda", 0)
+    o_ref, lse_ref = af.fwd(q.to(dev), k.to(dev), v.to(dev), mask, 0, 0.1)
+    torch.cuda.synchronize()
+    staging = {}
+    for _ in range(2):
+        o_h, lse_h = af.fwd_host(q, k, v, mask, 0, 0.1, staging=staging)
+        assert torch.equal(o_h, o_ref.cpu()) and torch.equal(lse_h, lse_ref.cpu())
+
+
 def test_argument_errors(af):
     dev = torch.device("cuda", 0)
     q = torch.zeros((1, 1, 256, 100), dtype=torch.float16, device=dev)
