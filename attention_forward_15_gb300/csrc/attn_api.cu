@@ -607,6 +607,7 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     prm.scale = sm_scale;
     prm.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634074);
     prm.d_out = D;
+    prm.inject = g_inject;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == ATTN_BF16;

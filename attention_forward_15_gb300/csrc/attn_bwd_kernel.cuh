@@ -57,6 +57,8 @@ struct BwdParams {
     float scale;             // sm_scale
     float scale_log2;        // sm_scale * log2(e)
     int d_out;               // head dim in memory (<= D of the kernel)
+    int inject;              // test hook: 1 = the producer issues no copies, so every
+                             // consumer's bounded wait runs out (0 in normal use)
 };
 
 // ------------------------------------------------------------------ prep
@@ -273,8 +275,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         // ================================================================ TMA producer
         uint32_t issued = 0;          // streamed stages issued
         bool fix_issued = false;
-        bool ok = true;
-        if (nn > 0) {
+        bool ok = p.inject != 1;
+        if (ok && nn > 0) {
             mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c) {
                 tma_load_3d(s_base + C::OFF_FIX + c * C::CHUNK_BYTES, &tm_f0, c * 64, f * 128, bh, bar(C::B_FIX));

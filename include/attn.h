@@ -205,7 +205,7 @@ int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size,
 
 /*
  * attn_debug_inject -- TEST HOOK, not for production use.  mode 1 makes every
- * following attn_fwd launch start with its copy-issuing warp doing nothing, so
+ * following attn_fwd or attn_bwd kernel start with its copy-issuing warp doing nothing, so
  * each consumer's bounded wait runs out after about one second: the kernel
  * records ATTN_ERR_TIMEOUT in the device status word, frees its tensor memory
  * and returns (outputs undefined), without hanging the GPU.  mode 0 restores

@@ -107,3 +107,29 @@ def test_plan_without_device(lib):
     assert p["units"] == 4 * 16 * 4 and p["threads"] == 352 and p["smem_bytes"] <= 232448
     p = af.plan(1, 16, 16384, 256, af.DENSE, dtype=__import__("torch").bfloat16, with_ctas=False)
     assert p["units"] == 16 * 128 and p["threads"] == 192
+
+
+def test_bwd_host_side(lib):
+    """attn_bwd's workspace size, work count and host-side argument checks (no
+    compute call: every case is rejected, or empty, before any CUDA call)."""
+    import attention_forward_15_gb300 as af
+    assert lib.attn_bwd_workspace_size(2, 3, 300) == 2 * 6 * 384 * 4     # rows padded to 128
+    assert lib.attn_bwd_workspace_size(1, 1, 0) == 0
+    assert lib.attn_bwd_workspace_size(-1, 1, 8) == 0
+    f, _ = af.bwd_work(2, 4, 512, 64, af.CAUSAL)
+    ff, _ = af.work(2, 4, 512, 64, af.CAUSAL)
+    assert f == 2.5 * ff
+
+    def b(D=64, L=256, ws=1 << 20, ptr=16, wsp=16, scale=0.1, mask=0, bs=0):
+        p = ctypes.c_void_p(ptr) if ptr else None
+        w = ctypes.c_void_p(wsp) if wsp else None
+        return lib.attn_bwd(p, p, p, p, p, p, p, p, p, w, ws, 1, 1, L, D, mask, bs, scale, 0, None)
+    assert b(D=256) == 4                      # no backward kernel past 128
+    assert b(D=100) == 4
+    assert b(ws=16) == 8                      # workspace too small
+    assert b(scale=float("nan")) == 8
+    assert b(ptr=0) == 1
+    assert b(wsp=0) == 1
+    assert b(ptr=24) == 5
+    assert b(mask=2, bs=48) == 3
+    assert b(L=0, ptr=0, wsp=0) == 0          # empty: nothing to do

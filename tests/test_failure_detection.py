@@ -53,3 +53,34 @@ def test_timeout_is_reported_and_recovered(af, D, mask, dt):
     assert np.abs(o.double().cpu().numpy() - O_ref).max() <= tol
     assert np.abs(lse.double().cpu().numpy() - l_ref).max() <= 1e-3
     assert af.last_device_status(0)[0] == 0
+
+
+def test_bwd_timeout_is_reported_and_recovered(af):
+    """The same for the backward's two tile kernels (one small head, so every
+    CTA's wait runs out at once): the timeout is reported with a wait site, and
+    the next backward on the same context is right."""
+    lib = af.load_library()
+    dev = torch.device("cuda", 0)
+    q, k, v = make_qkv(1, 1, 256, 64, torch.float16, seed=6)
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(7)).to(q.dtype)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    o, lse = af.fwd(qd, kd, vd, CAUSAL)
+    torch.cuda.synchronize()
+    assert af.last_device_status(0)[0] == 0
+    assert lib.attn_debug_inject(1) == 0
+    try:
+        af.bwd(qd, kd, vd, o, lse, gd, CAUSAL)
+        torch.cuda.synchronize()
+    finally:
+        assert lib.attn_debug_inject(0) == 0
+    st, detail = af.last_device_status(0)
+    assert st == 7, f"expected ATTN_ERR_TIMEOUT, got {st} (detail {detail:#x})"
+    assert (detail >> 8) & 0xff != 0
+    dq, dk, dv = af.bwd(qd, kd, vd, o, lse, gd, CAUSAL)
+    torch.cuda.synchronize()
+    assert af.last_device_status(0)[0] == 0
+    ref = oracle.attention_bwd(q, k, v, g, CAUSAL, 0, float(np.float32(1.0 / 8.0)), bounds=True)
+    u = 2.0 ** -11
+    for got, want, bnd in zip((dq, dk, dv), ref[:3], ref[3:]):
+        err = np.abs(got.double().cpu().numpy() - want)
+        assert (err <= 2.0 * u * (bnd + np.abs(want)) + 1e-6).all()
