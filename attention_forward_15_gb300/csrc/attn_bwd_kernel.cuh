@@ -18,7 +18,7 @@
 //     K and V of the tile stay in shared memory while the query tiles that
 //     attend it stream through a ring; per query tile
 //         S^T = K Q^T, dP^T = V dO^T       (tcgen05, fp32 in tensor memory)
-//         P^T, dS^T in the compute warps   (one thread per key row and half)
+//         P^T, dS^T in the compute warps   (one thread per key row and 32 columns)
 //         dV += P^T dO, dK += dS^T Q       (A operand from tensor memory)
 //   * attn_bwd_kernel<D, BF16, true> ("dQ"): one CTA per (head, query tile);
 //     Q and dO stay while the attended key tiles stream; per key tile
@@ -32,8 +32,9 @@
 // buffers of its own in tensor memory, so the MMA pipe computes one half's
 // products while the compute warps work on the other:
 //   S_0 | dP_0 | S_1 | dP_1 (64 columns each) | ACC0 (D) | ACC1 (D).
-// P (16-bit pairs) is written over the first 32 columns of its S and dS over
-// the first 32 of its dP, as the columns are consumed; a half's next S and dP
+// Each half is split between two warpgroups of 32 columns; a group writes its
+// P (16-bit pairs) over the first 16 of its S columns and its dS over the
+// first 16 of its dP columns, once read; a half's next S and dP
 // are issued after the products that read its P and dS, on the same in-order
 // MMA pipe.  D is 64 or 128 (256 + 2D columns).
 #pragma once
@@ -113,10 +114,10 @@ struct BwdCfg {
     static constexpr int CHUNK_BYTES = 128 * 128;
     static constexpr int TILE_BYTES = 128 * D * 2;
     static constexpr int NS = D == 64 ? 3 : 2;          // ring stages of streamed pairs
-    // two compute warpgroups (warps 0-3 take the first 64-row half of every
-    // streamed tile, warps 4-7 the second), a TMA warp and an MMA warp
-    static constexpr int THREADS = 320;
-    static constexpr int WARP_TMA = 8, WARP_MMA = 9;
+    // four compute warpgroups (group w takes 32 of the 64 rows of half w/2 of
+    // every streamed tile), a TMA warp and an MMA warp
+    static constexpr int THREADS = 576;
+    static constexpr int WARP_TMA = 16, WARP_MMA = 17;
     static constexpr int VEC_BYTES = DQ ? 0 : 2 * 128 * 4;   // -lse2 and -Di of one query tile
     static constexpr int OFF_FIX = 0;                        // F0 | F1
     static constexpr int OFF_RING = 2 * TILE_BYTES;          // NS x (R0 | R1)
@@ -157,19 +158,21 @@ __device__ __forceinline__ void bwd_range(const BwdParams &p, bool dq, int f, in
     }
 }
 
-// dS (and P) of one 32-column chunk: rows are this thread's TMEM lane, columns
-// c0..c0+31 of the tile.  S, dP: fp32 raw scores and dP of the chunk.  The
+// dS (and P) of one chunk of NE columns: rows are this thread's TMEM lane,
+// columns c0..c0+NE-1 of the tile.  S, dP: fp32 raw scores and dP of the chunk.  The
 // negated lse2 and Di come per row (dQ: nl_row, nd_row) or per column (dK/dV:
 // the shared-memory vectors, read four at a time); packed fp32x2 arithmetic as
 // in the forward; `keep` masks (row, column).
-template <bool BF16, bool DQ, bool MASKED>
-__device__ __forceinline__ void bwd_chunk(const uint32_t (&S)[32], const uint32_t (&dP)[32], float sc,
+template <bool BF16, bool DQ, bool MASKED, int NE>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&S)[NE], const uint32_t (&dP)[NE], float sc,
                                           float nl_row, float nd_row, const float *col_nl,
                                           const float *col_nd, int c0, int mask, int bs, int L,
-                                          int row_idx, int col_base, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+                                          int row_idx, int col_base, uint32_t (&pk)[NE / 2],
+                                          uint32_t (&dk)[NE / 2]) {
+    static_assert(NE % 4 == 0, "bwd_chunk: whole float4s of the column vectors");
     const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
+    for (int e = 0; e < NE / 2; ++e) {
         float2 nl, nd;
         if constexpr (DQ) {
             nl = make_float2(nl_row, nl_row);
@@ -239,7 +242,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar(C::B_SFULL + h), 1);
-            mbar_init(bar(C::B_PFULL + h), 4);   // one arrival per warp of half h's group
+            mbar_init(bar(C::B_PFULL + h), 8);   // one arrival per warp of half h's two groups
         }
         mbar_init(bar(C::B_DONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
@@ -329,13 +332,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             }
         };
         // ACC += A(TMEM, 16-bit pairs) B over 64 rows of B, B MN-major: k-step kk
-        // = rows [16kk, 16kk+16); its 64-column boxes are CHUNK_BYTES apart.
+        // = rows [16kk, 16kk+16); its 64-column boxes are CHUNK_BYTES apart.  The
+        // A pairs of rows [32g, 32g+32) sit at columns 32g..32g+15 of the half.
         auto issue_acc = [&](uint32_t acol, uint32_t b, uint32_t dcol, bool accumulate) {
             const uint64_t bd = sdesc_sw128(b, C::CHUNK_BYTES, 1024);
 #pragma unroll
             for (int kk = 0; kk < 64 / 16; ++kk)
-                mma_ts(tmem + dcol, tmem + acol + kk * 8, bd + static_cast<uint64_t>(kk * 128), IDESC_ACC,
-                       (accumulate || kk > 0) ? 1u : 0u);
+                mma_ts(tmem + dcol, tmem + acol + (kk >> 1) * 32 + (kk & 1) * 8,
+                       bd + static_cast<uint64_t>(kk * 128), IDESC_ACC, (accumulate || kk > 0) ? 1u : 0u);
         };
         // S_h and dP_h of the tile in ring stage `stage`
         auto issue_half = [&](int stage, int h) {
@@ -384,9 +388,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         __syncwarp();
     } else {
         // ================================================================ compute warps
-        // warpgroup h takes half h (rows 64h..64h+63 of every streamed tile);
-        // each thread owns one TMEM lane, i.e. one row of the fixed tile
-        const int h = warp >> 2;
+        // group wg takes columns [32g, 32g+32) of half h = wg/2 (g = wg%2) of every
+        // streamed tile; each thread owns one TMEM lane, i.e. one row of the
+        // fixed tile
+        const int wg = warp >> 2;
+        const int h = wg >> 1, g = wg & 1;
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int row_idx = f * 128 + row;                 // query (dQ) or key (dK/dV) index
@@ -396,6 +402,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             row_nl = p.nlse2[static_cast<size_t>(bh) * p.n_pad + row_idx];
             row_nd = p.ndelta[static_cast<size_t>(bh) * p.n_pad + row_idx];
         }
+        const uint32_t cs = tmem + lane_off + C::col_s(h) + 32 * g;    // this group's S columns
+        const uint32_t cd = tmem + lane_off + C::col_dp(h) + 32 * g;   // and dP columns
         bool ok = true;
         for (int t = 0; t < nn && ok; ++t) {
             const int s = t % C::NS;
@@ -407,28 +415,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             ok = wait_warp(bar(C::B_SFULL + h), t & 1, kSiteSFull);
             if (!ok) break;
             tc_fence_after();
-            // the half's S and dP in one round trip
-            uint32_t sv[64], dpv[64];
-            tmem_ld32(tmem + lane_off + C::col_s(h), *reinterpret_cast<uint32_t(*)[32]>(sv));
-            tmem_ld32(tmem + lane_off + C::col_s(h) + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-            tmem_ld32(tmem + lane_off + C::col_dp(h), *reinterpret_cast<uint32_t(*)[32]>(dpv));
-            tmem_ld32(tmem + lane_off + C::col_dp(h) + 32, *reinterpret_cast<uint32_t(*)[32]>(dpv + 32));
-            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t pk[16], dk[16];
-                const int c0 = 64 * h + 32 * c;     // column of the chunk in the tile
-                const uint32_t(&sc32)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + 32 * c);
-                const uint32_t(&dp32)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dpv + 32 * c);
+                uint32_t sv[16], dpv[16];
+                tmem_ld16(cs + 16 * c, sv);
+                tmem_ld16(cd + 16 * c, dpv);
+                tmem_wait_ld();
+                uint32_t pk[8], dk[8];
+                const int c0 = 64 * h + 32 * g + 16 * c;     // column of the sub-chunk in the tile
                 if (masked)
-                    bwd_chunk<BF16, DQ, true>(sc32, dp32, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
-                                              p.L, row_idx, j * 128, pk, dk);
+                    bwd_chunk<BF16, DQ, true, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
+                                                  p.L, row_idx, j * 128, pk, dk);
                 else
-                    bwd_chunk<BF16, DQ, false>(sc32, dp32, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
-                                               p.L, row_idx, j * 128, pk, dk);
-                // the whole half is in registers, so its columns may be overwritten
-                if constexpr (!DQ) tmem_st16(tmem + lane_off + C::col_s(h) + 16 * c, pk);
-                tmem_st16(tmem + lane_off + C::col_dp(h) + 16 * c, dk);
+                    bwd_chunk<BF16, DQ, false, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
+                                                   p.L, row_idx, j * 128, pk, dk);
+                // P and dS of sub-chunk c to columns [8c, 8c+8) of this group's
+                // S and dP columns, which it has read by now
+                if constexpr (!DQ) tmem_st8(cs + 8 * c, pk);
+                tmem_st8(cd + 8 * c, dk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -439,15 +443,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         if (ok && nn > 0) {
             tc_fence_after();
             const bool row_valid = row_idx < p.L;
-            // dK/dV: group 0 writes ACC1 (dK, times sm_scale) to g0, group 1 ACC0
-            // (dV) to g1; dQ: the groups split ACC1 (times sm_scale) by 32-column chunks
-            const bool to_g0 = DQ || h == 0;
-            const uint32_t acol = to_g0 ? C::COL_ACC1 : C::COL_ACC0;
-            const float mul = to_g0 ? p.scale : 1.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(to_g0 ? p.g0 : p.g1) +
-                                                   ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out) * 2);
+            // 32-column jobs: ACC1 (dK or dQ, times sm_scale) to g0, and (dK/dV)
+            // ACC0 (dV) to g1, dealt round-robin to the four groups
+            constexpr int NJ = (DQ ? 1 : 2) * (D / 32);
 #pragma unroll 1
-            for (int c = DQ ? h : 0; c < D / 32 && 32 * c < p.d_out; c += DQ ? 2 : 1) {
+            for (int jb = wg; jb < NJ; jb += 4) {
+                const bool to_g0 = jb < D / 32;
+                const int c = jb % (D / 32);
+                if (32 * c >= p.d_out) continue;
+                const uint32_t acol = to_g0 ? C::COL_ACC1 : C::COL_ACC0;
+                const float mul = to_g0 ? p.scale : 1.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(to_g0 ? p.g0 : p.g1) +
+                                                       ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out) * 2);
                 uint32_t raw[32];
                 tmem_ld32(tmem + lane_off + acol + 32 * c, raw);
                 tmem_wait_ld();
