@@ -226,9 +226,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // unit of this CTA: (head, fixed tile); causal units heaviest first
-    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
-    const int rank = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));
+    // unit of this CTA: (head, fixed tile).  Causal: heaviest fixed tiles first
+    // across all heads; otherwise head-major, so that CTAs running together
+    // stream the same head's tiles (shared in L2)
+    const bool head_major = p.mask != kMaskCausal;
+    const int bh = head_major ? static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_t))
+                              : static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
+    const int rank = head_major ? static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_t))
+                                : static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));
     const int f = (p.mask == kMaskCausal && DQ) ? p.n_t - 1 - rank : rank;
     int lo, hi;
     bwd_range(p, DQ, f, lo, hi);
