@@ -235,6 +235,7 @@ int attn_debug_inject(int mode);
  *                     reuse once the call's work on `stream` has completed.
  *   D                 a multiple of 8 from 8 to 128 (kernels for 64 and 128);
  *                     other arguments as for attn_fwd.
+ * Every pointer must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
  *
  * Three kernels run in order on `stream`.  Returns ATTN_OK once enqueued;
  * ATTN_ERR_ARG if workspace_bytes is too small or sm_scale is not finite;
