@@ -244,11 +244,26 @@ def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None
     if dist:
         dist.barrier()
     ms = e0.elapsed_time(e1) / steps
+    # Spread of the step time, outside the timed region: 30 replays of a graph
+    # of nsets steps (one pass over the rotating sets), each timed alone.
+    small = capture(nsets)
+    samples = []
+    for _ in range(30):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        small.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        samples.append(a.elapsed_time(b) / nsets)
+    samples.sort()
+    dist_ms = {"p10": round(samples[3], 5), "median": round(statistics.median(samples), 5),
+               "p90": round(samples[26], 5), "replays": 30, "steps_per_replay": nsets}
     st, det = af.last_device_status(dev.index)
     if st != 0:
         raise RuntimeError(f"device status {st} (detail {det:#x}) after the timed region")
     del graphs
-    return ms, {"rotating_sets": nsets, "set_bytes": per_set, "graph_launches": chunk}
+    return ms, {"rotating_sets": nsets, "set_bytes": per_set, "graph_launches": chunk,
+                "step_ms_spread": dist_ms}
 
 
 def time_bwd(af, w, dev, steps, warmup):
@@ -315,16 +330,16 @@ def time_e2e(af, w, dev, steps, warmup):
 
 # ----------------------------------------------------------------- oracle (CPU)
 
-def oracle_sample(w, n_heads: int, reps: int = 1):
+def oracle_sample(w, n_heads: int, reps: int = 1, threads: int | None = None):
     """Time the CPU fp64 oracle on the first n_heads (b, h) heads of workload
-    w (all rows of each), reps times over; returns (seconds, flops of the
-    sample, threads)."""
+    w (all rows of each), reps times over, on `threads` host threads (default
+    all); returns (seconds, flops of the sample, threads)."""
     import oracle
     q, k, v = make_workload_inputs(w)
     BH = w.B * w.H
     n_heads = max(1, min(n_heads, BH))
     qf, kf, vf = (t.reshape(BH, 1, w.L, w.D)[:n_heads].contiguous() for t in (q, k, v))
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     oracle.load()
     t0 = time.perf_counter()
     for _ in range(reps):
@@ -353,8 +368,12 @@ def cpu_baseline(w, target_s: float = 10.0):
     what = f"all {w.L} rows of {n} of the {w.B * w.H} (b,h) heads"
     if reps > 1:
         what += f", the whole workload {reps} times"
+    # the same oracle on one thread, one head
+    dt_1t, f_1t, _ = oracle_sample(w, 1, threads=1)
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{what}, fp64, {dt:.2f} s wall"}
+            "sample": f"{what}, fp64, {dt:.2f} s wall",
+            "single_thread": {"value": f_1t / dt_1t / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"all {w.L} rows of 1 (b,h) head, fp64, {dt_1t:.2f} s wall"}}
 
 
 # ----------------------------------------------------------------- ranks
@@ -498,6 +517,7 @@ def main():
                       f"{info['set_bytes'] / 2**20:.1f} MiB (> 2x the 129 MB L2)",
                 "launch": f"CUDA graph replay of {info['graph_launches']} launches",
                 "flops_per_step": flops, "bytes_per_step": nbytes,
+                "step_ms_spread": info["step_ms_spread"],
                 "clocks_note": f"sampled over a {args.soak_s:.1f} s soak of the same graph "
                                "immediately before the timed region"})
     out = {
@@ -530,7 +550,7 @@ def run_reference(args, w, world):
     import attention_forward_15_gb300 as af   # for the work count only (host function)
     q, k, v = make_workload_inputs(w)
     BH = w.B * w.H
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     oracle.load()
     heads = [t.reshape(BH, 1, w.L, w.D) for t in (q, k, v)]
 
