@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only the backward (attn_bwd) on --workload and print one line "
                          "(for profiler runs)")
+    ap.add_argument("--threads", type=int, default=None,
+                    help="host threads of the CPU oracle (--impl reference and the CPU baseline; "
+                         "default: every core)")
     ap.add_argument("--lean", action="store_true",
                     help="only the device-timed line: no soak, e2e, CPU baseline or other "
                          "workloads (for profiler runs)")
@@ -161,14 +164,9 @@ def rotation_sets(w, dev, nbytes_set):
 
 
 def make_device_inputs(w, dev):
-    if w.name == HEADLINE:
-        return tuple(t.to(dev) for t in make_workload_inputs(w))   # the seeded CPU recipe
-    # same distribution, drawn on the device (faster for the large workloads)
-    g = torch.Generator(device=dev)
-    g.manual_seed(w.seed)
-    shape = (w.B, w.H, w.L, w.D)
-    return tuple(torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
-                 .mul_(w.std).to(w.dtype) for _ in range(3))
+    """The workload's inputs from the seeded CPU recipe (the same values the
+    parity tests check), copied to the device."""
+    return tuple(t.to(dev) for t in make_workload_inputs(w))
 
 
 def time_workload(af, w, dev, steps, warmup, soak_s=0.0, sampler=None, dist=None, fp8v=False):
@@ -313,8 +311,7 @@ def time_bwd(af, w, dev, steps, warmup):
 def time_e2e(af, w, dev, steps, warmup):
     """End to end through the public host API: each step copies q, k, v from
     pinned host memory, runs the forward and copies o and lse back."""
-    q, k, v = (t.pin_memory() for t in make_workload_inputs(w)) if w.name == HEADLINE else \
-        (t.cpu().pin_memory() for t in make_device_inputs(w, dev))
+    q, k, v = (t.pin_memory() for t in make_workload_inputs(w))
     staging: dict = {}
     for _ in range(max(warmup, 1)):
         af.fwd_host(q, k, v, w.mask, w.block_size, w.sm_scale, device=dev.index, staging=staging)
@@ -543,14 +540,23 @@ def main():
         dist.destroy_process_group()
 
 
+def attended_pairs(w) -> float:
+    """Attended (i, j) pairs of one head: L^2 dense, L(L+1)/2 causal, L*bs
+    block-diagonal."""
+    if w.mask == 0:
+        return float(w.L) * w.L
+    if w.mask == 1:
+        return w.L * (w.L + 1) / 2.0
+    return float(w.L) * w.block_size
+
+
 def run_reference(args, w, world):
     """The oracle as the reference arm: each step computes one (b,h) head of
     the workload in fp64 on the host cores."""
     import oracle
-    import attention_forward_15_gb300 as af   # for the work count only (host function)
     q, k, v = make_workload_inputs(w)
     BH = w.B * w.H
-    threads = threads or os.cpu_count() or 1
+    threads = args.threads or os.cpu_count() or 1
     oracle.load()
     heads = [t.reshape(BH, 1, w.L, w.D) for t in (q, k, v)]
 
@@ -564,7 +570,7 @@ def run_reference(args, w, world):
     for i in range(args.steps):
         step(i)
     dt = (time.perf_counter() - t0) / args.steps
-    f_head, _ = af.work(1, 1, w.L, w.D, w.mask, w.block_size, w.dtype)
+    f_head = 4.0 * w.D * attended_pairs(w)
     value = f_head / dt / 1e12
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
