@@ -46,6 +46,14 @@ _SIGNATURES = {
     "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_size_t] + [ctypes.c_int] * 6 +
                  [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 3),
+    "attn_fwd_check": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
+                       [ctypes.c_float, ctypes.c_int]),
+    "attn_fwd_fp8v_check": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
+                            [ctypes.c_float, ctypes.c_int]),
+    "attn_bwd_check": (ctypes.c_int, [ctypes.c_void_p] * 10 + [ctypes.c_size_t] + [ctypes.c_int] * 6 +
+                       [ctypes.c_float, ctypes.c_int]),
+    "attn_fwd_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
+                         [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "attn_bwd_work": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_double)] * 2),
 }
 

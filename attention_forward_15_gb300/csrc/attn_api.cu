@@ -213,7 +213,7 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
 
 extern "C" {
 
-int attn_abi_version(void) { return (1 << 16) | 0; }
+int attn_abi_version(void) { return (1 << 16) | 1; }
 
 int attn_debug_inject(int mode) {
     if (mode != 0 && mode != 1) return ATTN_ERR_ARG;
@@ -276,11 +276,14 @@ int attn_fwd_plan(int B, int H, int L, int D, int mask_kind, int block_size, int
 
 namespace {
 
-// attn_fwd and attn_fwd_fp8v: validation, plan, parameters and the launch of the
-// kernel for the head dim (FP8V: V given as e5m2 V^T).
+// The host-side checks of a forward call (attn_fwd, attn_fwd_noalloc,
+// attn_fwd_fp8v with FP8V): no CUDA call and no access to the buffers.
+// *launch is set to false for an empty problem (nothing to enqueue).
 template <bool FP8V>
-int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
-               int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+int check_fwd_args(const void *q, const void *k, const void *v, const void *o, const void *lse, int B,
+                   int H, int L, int D, int mask_kind, int block_size, float sm_scale, int dtype,
+                   bool *launch) {
+    *launch = false;
     int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
     if (rc != ATTN_OK) return rc;
     if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
@@ -288,9 +291,20 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     if (FP8V && L % 16 != 0) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-        (lse && (reinterpret_cast<uintptr_t>(lse) & 15u) != 0))
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
         return ATTN_ERR_ALIGN;
+    *launch = true;
+    return ATTN_OK;
+}
+
+// attn_fwd and attn_fwd_fp8v: validation, plan, parameters and the launch of the
+// kernel for the head dim (FP8V: V given as e5m2 V^T).
+template <bool FP8V>
+int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
+               int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+    bool go = false;
+    int rc = check_fwd_args<FP8V>(q, k, v, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, &go);
+    if (rc != ATTN_OK || !go) return rc;
 
     DeviceState *st = nullptr;
     rc = device_state(&st, nullptr);
@@ -331,6 +345,19 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
 }  // namespace
 
 extern "C" {
+
+int attn_fwd_check(const void *q, const void *k, const void *v, const void *o, const float *lse, int B,
+                   int H, int L, int D, int mask_kind, int block_size, float sm_scale, int dtype) {
+    bool go = false;
+    return check_fwd_args<false>(q, k, v, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, &go);
+}
+
+int attn_fwd_fp8v_check(const void *q, const void *k, const void *vt, const void *o, const float *lse,
+                        int B, int H, int L, int D, int mask_kind, int block_size, float sm_scale,
+                        int dtype) {
+    bool go = false;
+    return check_fwd_args<true>(q, k, vt, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, &go);
+}
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int L,
              int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
@@ -447,20 +474,16 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, voi
                                 int B, int H, int L, int D, int mask_kind, int block_size,
                                 float sm_scale, int dtype, void *stream,
                                 unsigned int *status_out) {
-    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
+    bool go = false;
+    int rc = check_fwd_args<false>(q, k, v, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, &go);
     if (rc != ATTN_OK) return rc;
-    if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
     // scratch this kernel needs: one status word, whatever the problem size
     constexpr size_t kNeeded = sizeof(unsigned int);
     if (kNeeded > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * H * L == 0) {
+    if (!go) {
         if (status_out) *status_out = 0;
         return ATTN_OK;
     }
-    if (!q || !k || !v || !o) return ATTN_ERR_NULL;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-        (lse && (reinterpret_cast<uintptr_t>(lse) & 15u) != 0))
-        return ATTN_ERR_ALIGN;
 
     DeviceState *st = nullptr;
     rc = noalloc_state(&st);
@@ -572,9 +595,10 @@ size_t attn_bwd_workspace_size(int B, int H, int L) {
     return bwd_workspace_bytes(static_cast<long long>(B) * H, L);
 }
 
-int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
-             void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, int B, int H, int L, int D,
-             int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+int attn_bwd_check(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, const void *dq, const void *dk, const void *dv, const void *workspace,
+                   size_t workspace_bytes, int B, int H, int L, int D, int mask_kind, int block_size,
+                   float sm_scale, int dtype) {
     int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
     if (rc != ATTN_OK) return rc;
     if (D > 128) return ATTN_ERR_UNSUPPORTED;
@@ -584,8 +608,18 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
         !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
         return ATTN_ERR_ALIGN;
+    if (workspace_bytes < bwd_workspace_bytes(static_cast<long long>(B) * H, L)) return ATTN_ERR_ARG;
+    return ATTN_OK;
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+             void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, int B, int H, int L, int D,
+             int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
+    int rc = attn_bwd_check(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, L, D,
+                            mask_kind, block_size, sm_scale, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
     const long long bh = static_cast<long long>(B) * H;
-    if (workspace_bytes < bwd_workspace_bytes(bh, L)) return ATTN_ERR_ARG;
 
     DeviceState *st = nullptr;
     rc = device_state(&st, nullptr);

@@ -83,12 +83,14 @@ typedef enum {
  * the stream is synchronised.  The kernel is launched as a programmatic
  * dependent of the previous kernel on `stream` (its CTAs may be scheduled
  * while that kernel finishes, but they wait for its completion before any
- * global memory access), so stream ordering is unchanged for the caller.  Argument errors are detected on the host
- * before any CUDA call and nothing is launched or written.  A failed launch
- * returns ATTN_ERR_CUDA.  Every wait inside the kernel is bounded (about one
- * second); if one runs out the kernel stops, frees its tensor memory and
- * records ATTN_ERR_TIMEOUT in a per-device status word that
- * attn_last_device_status() reads.  Reentrant; safe from several host threads.
+ * global memory access), so stream ordering is unchanged for the caller.
+ * Argument errors are detected on the host before any CUDA call
+ * (attn_fwd_check runs the same checks alone) and nothing is launched or
+ * written.  A failed launch returns ATTN_ERR_CUDA.  Every wait inside the
+ * kernel is bounded (about one second); if one runs out the kernel stops,
+ * frees its tensor memory and records ATTN_ERR_TIMEOUT in a per-device status
+ * word that attn_last_device_status() reads.  Reentrant; safe from several
+ * host threads.
  */
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int L, int D, int mask_kind, int block_size,
@@ -104,6 +106,20 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  */
 int attn_fwd_work(int B, int H, int L, int D, int mask_kind, int block_size,
                   int dtype, double *flops, double *bytes);
+
+/*
+ * attn_fwd_check -- the host-side argument checks of attn_fwd (and of
+ * attn_fwd_noalloc, which runs the same ones), alone: the same arguments
+ * without the stream, the same status attn_fwd would return before any CUDA
+ * call (ATTN_OK for an empty problem or for arguments that pass).  It makes no
+ * CUDA call and never reads or writes through the pointers, which are only
+ * tested for NULL and for 16-byte alignment; so a caller (or a test) may
+ * check arguments on a machine without a GPU, or with addresses that are not
+ * allocated, without anything being launched.
+ */
+int attn_fwd_check(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   int B, int H, int L, int D, int mask_kind, int block_size,
+                   float sm_scale, int dtype);
 
 /* Human-readable name of an attn_status (static storage; never NULL). */
 const char *attn_status_string(int status);
@@ -171,6 +187,12 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
 int attn_fwd_fp8v(const void *q, const void *k, const void *vt, void *o, float *lse,
                   int B, int H, int L, int D, int mask_kind, int block_size,
                   float sm_scale, int dtype, void *stream);
+
+/* The host-side argument checks of attn_fwd_fp8v alone (as attn_fwd_check:
+ * no CUDA call, the pointers never dereferenced). */
+int attn_fwd_fp8v_check(const void *q, const void *k, const void *vt, const void *o,
+                        const float *lse, int B, int H, int L, int D, int mask_kind,
+                        int block_size, float sm_scale, int dtype);
 
 /*
  * attn_fwd_host -- the whole forward for inputs and outputs in HOST memory:
@@ -246,6 +268,13 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
              const float *lse, void *dq, void *dk, void *dv, void *workspace,
              size_t workspace_bytes, int B, int H, int L, int D, int mask_kind,
              int block_size, float sm_scale, int dtype, void *stream);
+
+/* The host-side argument checks of attn_bwd alone (as attn_fwd_check: no
+ * CUDA call, the pointers never dereferenced). */
+int attn_bwd_check(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, const void *dq, const void *dk, const void *dv,
+                   const void *workspace, size_t workspace_bytes, int B, int H, int L, int D,
+                   int mask_kind, int block_size, float sm_scale, int dtype);
 
 /* Bytes of workspace attn_bwd needs: two fp32 values per row, rows padded to
  * whole 128-row tiles per head (0 for negative sizes). */

@@ -66,9 +66,14 @@ def test_noalloc_matches_regular_entry_point(lib, case):
 
 
 def test_noalloc_rejects_bad_arguments(lib):
-    # placeholder pointers: every call here must be rejected on the host
-    rc = lib.attn_fwd_noalloc(16, 16, 16, 16, None, 1, 1, 256, 100, DENSE, 0, 0.1, 0, None, None)
-    assert rc == 4                                    # head dim not a multiple of 8
-    rc = lib.attn_fwd_noalloc(16, 16, 16, 16, None, 1, 1, 256, 64, BLOCK_DIAG, 48, 0.1, 0,
-                              None, None)
-    assert rc == 3
+    """Calls that must be refused on the host.  The buffers are real device
+    allocations of the size each call describes, so that even a call that
+    wrongly got through would stay inside memory it owns."""
+    dev = torch.device("cuda", 0)
+    for (B, H, L, D, mask, bs), want in (((1, 1, 256, 100, DENSE, 0), 4),       # D not a multiple of 8
+                                         ((1, 1, 256, 64, BLOCK_DIAG, 48), 3)):  # 48 does not divide 256
+        q, k, v, o = (torch.zeros((B, H, L, D), dtype=torch.float16, device=dev) for _ in range(4))
+        rc = lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None,
+                                  B, H, L, D, mask, bs, 0.1, 0, None, None)
+        assert rc == want
+    torch.cuda.synchronize()
