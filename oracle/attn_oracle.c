@@ -340,6 +340,9 @@ static void one_row_fp8v(const double *q, const double *k, const uint8_t *vt, lo
             l += p;
 #endif
             double vmax = 0.0;
+#if ORACLE_MUTANT == 15
+            double vsum = 0.0;
+#endif
             for (long d = 0; d < D; ++d) {
 #if ORACLE_MUTANT == 13
                 const double vj = widen_e5m2(vt[j * D + d]);   /* planted: V read untransposed */
@@ -348,13 +351,25 @@ static void one_row_fp8v(const double *q, const double *k, const uint8_t *vt, lo
 #endif
                 o[d] += p8 * vj;
                 if (fabs(vj) > vmax) vmax = fabs(vj);
+#if ORACLE_MUTANT == 15
+                vsum += fabs(vj);
+#endif
             }
             /* p within the single-precision error of a tie (relative band
-             * delta, see above) may round to the other neighbour */
-            const double delta = (double)D * 0x1p-24 * s[L + j] +
-                                 0x1p-23 * (fabs(s[j]) + fabs(m_new)) + 5e-5;
+             * delta, see above) may round to the other neighbour; one such
+             * flip moves each element of O by qv |v_jd| / l, so the row's
+             * largest change is qv max_d |v_jd| / l */
+            double delta = (double)D * 0x1p-24 * s[L + j] +
+                           0x1p-23 * (fabs(s[j]) + fabs(m_new)) + 5e-5;
+#if ORACLE_MUTANT == 14
+            delta *= 100.0;                            /* planted: band 100x too wide */
+#endif
             const double frac = p / qv - floor(p / qv);
+#if ORACLE_MUTANT == 15
+            if (fabs(frac - 0.5) < delta * (p / qv)) tie += qv * vsum;   /* planted: per column */
+#else
             if (fabs(frac - 0.5) < delta * (p / qv)) tie += qv * vmax;
+#endif
         }
         m = m_new;
     }
@@ -497,9 +512,21 @@ static void one_head_bwd(const double *q, const double *k, const double *v, cons
 #else
                 dK[j * D + d] += sm_scale * dS[j] * q[i * D + d];
 #endif
-                if (bV) bV[j * D + d] += P[j] * fabs(dOi[d]);
+#if ORACLE_MUTANT == 24
+                if (bQ) bQ[i * D + d] += 4.0 * fabs(sm_scale) * w * fabs(k[j * D + d]);  /* planted: 4x */
+#else
                 if (bQ) bQ[i * D + d] += fabs(sm_scale) * w * fabs(k[j * D + d]);
+#endif
+#if ORACLE_MUTANT == 25
+                if (bK) bK[j * D + d] += 4.0 * fabs(sm_scale) * w * fabs(q[i * D + d]);  /* planted: 4x */
+#else
                 if (bK) bK[j * D + d] += fabs(sm_scale) * w * fabs(q[i * D + d]);
+#endif
+#if ORACLE_MUTANT == 26
+                if (bV) bV[j * D + d] += 4.0 * P[j] * fabs(dOi[d]);                      /* planted: 4x */
+#else
+                if (bV) bV[j * D + d] += P[j] * fabs(dOi[d]);
+#endif
             }
         }
     }

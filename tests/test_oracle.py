@@ -447,8 +447,123 @@ def _fp8_pin_running_max_across_tiles(mutant):
     assert abs(O[0, 0, 0, 0] - want) <= 1e-9, (O[0, 0, 0, 0], want)
 
 
+# The oracle's per-row ``slack`` widens the FP8 parity tolerance, so it is
+# pinned from above as well as from below: it is zero where no p lies near an
+# e5m2 rounding tie, it is exactly one tie's worth where one p sits on a tie,
+# and on random inputs it stays under a closed-form bound the test computes
+# from its own scores.
+
+def _e5m2_quantum(p: float) -> float:
+    """Spacing of float8 e5m2 values around p (2 fraction bits; subnormal
+    spacing 2^-16 below 2^-14), from the format's definition."""
+    if p < 2.0 ** -14:
+        return 2.0 ** -16
+    return 2.0 ** (math.floor(math.log2(p)) - 2)
+
+
+def _split_score_keys(targets):
+    """fp16 key rows [x, r] whose scores x + r (with q = [1, 1], scale 1) hit
+    ln(target) to about 1e-6: x is the nearest fp16 and r the fp16 residual."""
+    rows = []
+    for t in targets:
+        z = math.log(t)
+        x = float(torch.tensor(z, dtype=torch.float16))
+        r = float(torch.tensor(z - x, dtype=torch.float16))
+        rows.append((x, r))
+    return rows
+
+
+def _fp8_pin_slack_zero_off_ties(mutant):
+    """No p near a tie, so no rounding decision is in doubt and slack is 0:
+    (a) Q = 0, every p exactly 1; (b) keys whose p lie 0.008 to 0.016 of a
+    quantum from the midpoint between two e5m2 neighbours -- far outside the
+    single-precision error of the exponent (below 1e-6 relative here, plus 5e-5
+    for an approximate exponential, i.e. under 4e-4 of a quantum)."""
+    B, H, L, D = 1, 2, 256, 8
+    g = torch.Generator().manual_seed(4)
+    q = torch.zeros(B, H, L, D, dtype=torch.float16)
+    k = torch.randn(B, H, L, D, generator=g).to(torch.float16)
+    vt = (torch.randn(B, H, D, L, generator=g) * 2).to(torch.float8_e5m2)
+    for mask, bs in ((DENSE, 0), (CAUSAL, 0), (BLOCK_DIAG, 64)):
+        _, _, slack = _fp8_run(mutant, q, k, vt, mask, bs)
+        assert (slack == 0.0).all(), slack.max()
+    # (b): midpoints (n + 1/2) qv of the binades [1/16, 1), each missed by
+    # 0.012 of a quantum on either side
+    targets = []
+    for e in range(-4, 0):
+        qv = 2.0 ** (e - 2)
+        for n in range(4, 8):
+            for side in (-1, 1):
+                targets.append((n + 0.5 + side * 0.012) * qv)
+    keys = [(0.0, 0.0)] + _split_score_keys(targets)       # key 0: score 0, the row max
+    L = len(keys)
+    kk = torch.tensor(keys, dtype=torch.float16).view(1, 1, L, 2)
+    qq = torch.ones(1, 1, L, 2, dtype=torch.float16)
+    for x, r in keys[1:]:                                   # the test's own check of each p
+        p = math.exp(x + r)
+        qv = _e5m2_quantum(p)
+        dist = abs(p / qv - math.floor(p / qv) - 0.5)
+        assert 0.008 <= dist <= 0.016, (p, dist)
+    vt = torch.linspace(-3, 3, 2 * L).view(1, 1, 2, L).to(torch.float8_e5m2)
+    _, _, slack = _fp8_run(mutant, qq, kk, vt)
+    assert (slack == 0.0).all(), slack.max()
+
+
+def _fp8_pin_slack_at_exact_tie(mutant):
+    """Key 1's p sits on the e5m2 tie 0.9375 (between 0.875 and 1) to about
+    1e-6: rounding it either way is correct, and the largest change of an
+    element of O that the choice makes is qv max_d |v_1d| / l with qv = 1/8 --
+    which is what slack must be, exactly (one key, counted once, by the largest
+    element of its V row)."""
+    (x, r), = _split_score_keys([0.9375])
+    kk = torch.tensor([[0.0, 0.0], [x, r]], dtype=torch.float16).view(1, 1, 2, 2)
+    qq = torch.ones(1, 1, 2, 2, dtype=torch.float16)
+    p1 = math.exp(x + r)
+    assert abs(p1 / 0.9375 - 1.0) <= 2e-6
+    v1 = (2.0, -1.5, 0.75)                                 # exact in e5m2
+    vt = torch.tensor([[1.0, v1[0]], [0.5, v1[1]], [-1.0, v1[2]]]).to(torch.float8_e5m2).view(1, 1, 3, 2)
+    vt = vt.view(torch.uint8)
+    kk3 = torch.cat([kk, torch.zeros(1, 1, 2, 1, dtype=torch.float16)], dim=-1)
+    qq3 = torch.cat([qq, torch.zeros(1, 1, 2, 1, dtype=torch.float16)], dim=-1)
+    _, _, slack = _fp8_run(mutant, qq3, kk3, vt)
+    want = 0.125 * max(abs(x) for x in v1) / (1.0 + p1)
+    assert np.abs(slack - want).max() <= 1e-12 * want, (slack, want)
+
+
+def _fp8_pin_slack_closed_form_bound(mutant):
+    """Random N(0,1) inputs, one 128-key tile (so the running max is the row
+    max): slack <= sum over the keys whose p lies within 2e-4 p (a stated bound
+    of the single-precision error of the exponent on these inputs: D 2^-24
+    sum|q k| scale is below 4e-5, plus 5e-5 for an approximate exponential) of
+    a tie of qv max_d |v_jd| / l, with p, qv, l computed here in fp64 from the
+    widened inputs."""
+    B, H, L, D = 1, 4, 128, 64
+    scale = 0.125
+    q, k, v = make_qkv(B, H, L, D, torch.float16, seed=17)
+    vt = v.float().to(torch.float8_e5m2).transpose(-1, -2).contiguous()
+    _, _, slack = _fp8_run(mutant, q, k, vt, DENSE, 0, scale)
+    s = (q.double() @ k.double().transpose(-1, -2)).numpy() * scale
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    l = p.sum(axis=-1)
+    vmax = np.abs(vt.double().numpy()).max(axis=-2)                 # [B, H, L] per key
+    bound = np.zeros_like(l)
+    n_near = 0
+    for b in range(B):
+        for h in range(H):
+            for i in range(L):
+                for j in range(L):
+                    qv = _e5m2_quantum(p[b, h, i, j])
+                    t = p[b, h, i, j] / qv
+                    if abs(t - math.floor(t) - 0.5) < 2e-4 * t:
+                        bound[b, h, i] += qv * vmax[b, h, j] / l[b, h, i]
+                        n_near += 1
+    assert (slack <= bound + 1e-15).all(), (slack - bound).max()
+    assert n_near < 0.01 * B * H * L * L        # the bound itself is not vacuous
+
+
 FP8_PINS = [_fp8_pin_top_byte_of_f16, _fp8_pin_rounding_brute_force, _fp8_pin_uniform_scores,
-            _fp8_pin_rounded_weights, _fp8_pin_running_max_across_tiles]
+            _fp8_pin_rounded_weights, _fp8_pin_running_max_across_tiles, _fp8_pin_slack_zero_off_ties,
+            _fp8_pin_slack_at_exact_tie, _fp8_pin_slack_closed_form_bound]
 
 
 @pytest.mark.parametrize("pin", FP8_PINS, ids=lambda f: f.__name__)
@@ -460,6 +575,8 @@ FP8_MUTANTS = {
     11: "e5m2 rounding truncates",
     12: "denominator sums the rounded p",
     13: "V read untransposed",
+    14: "tie band 100x too wide",
+    15: "tie counted per column",
 }
 
 
@@ -551,8 +668,57 @@ def _bwd_pin_block_size_one(mutant):
     assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0
 
 
+# The magnitudes bQ, bK, bV scale the backward's parity tolerance, so they are
+# pinned from above: on inputs where the triangle inequality behind them is an
+# equality they must equal |dQ|, |dK|, |dV|, and block size 1 gives each in
+# closed form.
+
+def _bwd_pin_bound_of_dv_is_tight(mutant):
+    """dO >= 0 everywhere: every term P[i,j] dO[i,d] of dV[j,d] is >= 0, so
+    bV = sum_i P[i,j] |dO[i,d]| equals |dV| exactly (every mask)."""
+    for mask, bs in BWD_MASKS:
+        q, k, v, g = _bwd_inputs(110 + mask, L=15, D=5)
+        g = g.abs()
+        _, _, dv, _, _, bv = oracle.attention_bwd(q, k, v, g, mask, bs, 0.8, bounds=True, mutant=mutant)
+        assert np.abs(bv - np.abs(dv)).max() <= 1e-12 * max(1.0, np.abs(dv).max())
+
+
+def _bwd_pin_bounds_tight_on_two_keys(mutant):
+    """Two keys k = (a, -a), both queries 1 (one head dim), so each row has the
+    weights (w, 1 - w), w = 1/(1 + exp(-2 s a)); V = c (1 - w, -w) makes O = 0,
+    so the row terms a_i = sum_d |dO O| and D_i vanish and dS[i] = c w (1 - w)
+    dO_i (1, -1).  Then dQ_i = 2 s a dS[i,0] with every term of bQ of one sign,
+    and with dO = (1, 2) (one sign) the same holds for dK: bQ = |dQ| and
+    bK = |dK| exactly, and bV = |dV| (dO >= 0)."""
+    for a, scale, c in ((0.7, 0.9, 1.5), (-1.2, 0.4, -0.8), (0.3, -2.0, 2.5)):
+        w = 1.0 / (1.0 + math.exp(-2.0 * scale * a))
+        q = torch.ones(1, 1, 2, 1, dtype=torch.float64)
+        k = torch.tensor([a, -a], dtype=torch.float64).view(1, 1, 2, 1)
+        v = torch.tensor([c * (1 - w), -c * w], dtype=torch.float64).view(1, 1, 2, 1)
+        g = torch.tensor([1.0, 2.0], dtype=torch.float64).view(1, 1, 2, 1)
+        dq, dk, dv, bq, bk, bv = oracle.attention_bwd(q, k, v, g, DENSE, 0, scale, bounds=True, mutant=mutant)
+        ds0 = c * w * (1 - w) * np.array([1.0, 2.0])          # dS[i, 0] of rows 0, 1
+        assert np.abs(dq.reshape(2) - 2 * scale * a * ds0).max() <= 1e-12
+        for x, bx in ((dq, bq), (dk, bk), (dv, bv)):
+            assert np.abs(bx - np.abs(x)).max() <= 1e-12 * max(1.0, np.abs(x).max()), (x, bx)
+
+
+def _bwd_pin_bounds_block_size_one(mutant):
+    """Block size 1: P = 1 on the diagonal, dS = 0, O_i = v_i, so bV = |dO|,
+    bQ[i,d] = |s| a_i |k[i,d]| and bK[i,d] = |s| a_i |q[i,d]| with
+    a_i = sum_d |dO[i,d] v[i,d]|."""
+    q, k, v, g = _bwd_inputs(120, L=9, D=4)
+    scale = -0.7
+    _, _, _, bq, bk, bv = oracle.attention_bwd(q, k, v, g, BLOCK_DIAG, 1, scale, bounds=True, mutant=mutant)
+    a = (g * v).abs().sum(dim=-1, keepdim=True).numpy()
+    assert np.abs(bv - g.abs().numpy()).max() <= 1e-15
+    assert np.abs(bq - abs(scale) * a * k.abs().numpy()).max() <= 1e-12
+    assert np.abs(bk - abs(scale) * a * q.abs().numpy()).max() <= 1e-12
+
+
 BWD_PINS = [_bwd_pin_finite_differences, _bwd_pin_torch_autograd, _bwd_pin_invariants,
-            _bwd_pin_block_size_one]
+            _bwd_pin_block_size_one, _bwd_pin_bound_of_dv_is_tight, _bwd_pin_bounds_tight_on_two_keys,
+            _bwd_pin_bounds_block_size_one]
 
 
 @pytest.mark.parametrize("pin", BWD_PINS, ids=lambda f: f.__name__)
@@ -564,6 +730,9 @@ BWD_MUTANTS = {
     21: "row term Di dropped from dS",
     22: "sm_scale dropped from dK",
     23: "P transposed in dV",
+    24: "bound of dQ 4x too large",
+    25: "bound of dK 4x too large",
+    26: "bound of dV 4x too large",
 }
 
 
