@@ -169,7 +169,7 @@ int encode_map_vt8(CUtensorMap *m, const void *ptr, int BH, int L, int D, int ro
 template <int D, bool BF16, bool PAIR, bool FP8V = false>
 int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdParams prm, int dtype,
            cudaStream_t stream) {
-    using C = Cfg<D, PAIR>;
+    using C = Cfg<D, PAIR, FP8V>;
     auto kern = attn::attn_fwd_kernel<D, BF16, PAIR, FP8V>;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
@@ -178,6 +178,15 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM_BYTES) != cudaSuccess)
                 return ATTN_ERR_CUDA;
+            if constexpr (C::REGSPLIT) {
+                // The kernel moves registers between warpgroups (setmaxnreg); the
+                // split assumes the block's pool is THREADS x REGS_LAUNCH.  A
+                // smaller pool would leave the increase waiting forever, so such a
+                // build is refused here rather than launched.
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_CUDA;
+                if (fa.numRegs != C::REGS_LAUNCH) return ATTN_ERR_UNSUPPORTED;
+            }
             set = true;
         }
     }

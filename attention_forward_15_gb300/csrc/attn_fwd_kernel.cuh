@@ -74,7 +74,7 @@ struct FwdParams {
                              // the columns past it load as zeros and are not stored)
 };
 
-template <int D, bool PAIR>
+template <int D, bool PAIR, bool FP8V = false>
 struct Cfg {
     static constexpr int NQ = PAIR ? 2 : 1;           // query tiles resident per CTA
     static constexpr int NWG = PAIR ? 2 : 1;          // softmax warpgroups
@@ -92,14 +92,26 @@ struct Cfg {
     // Then a second MMA warp issues the P.V products, so that neither issuer's
     // barrier waits hold back the other's MMAs.
     static constexpr bool SEP = PAIR && D == 64;
-    static constexpr int NUM_WARPS = 4 * NWG + 2 + (SEP ? 1 : 0);
+    // REGSPLIT (the FP8 P.V variant in the separate-P mode): the copy and MMA
+    // warps fill a whole fourth warpgroup (one warp idle) so that registers can
+    // move between warpgroups, and the softmax warpgroups hold a whole S row
+    // and the row's packed P in registers (measured faster there; the 16-bit
+    // separate-P mode measured faster without it).
+    static constexpr bool REGSPLIT = SEP && FP8V;
+    static constexpr int NUM_WARPS = REGSPLIT ? 12 : 4 * NWG + 2 + (SEP ? 1 : 0);
     static constexpr int THREADS = 32 * NUM_WARPS;
     static constexpr int WARP_TMA = 4 * NWG;
     static constexpr int WARP_MMA = 4 * NWG + 1;
     static constexpr int WARP_PV = 4 * NWG + 2;     // SEP only
+    // REGSPLIT register split (per thread): launched with REGS_LAUNCH, the
+    // copy/MMA warpgroup drops to REGS_CTRL and the softmax warpgroups rise to
+    // REGS_SOFT; the two splits use the same total.
+    static constexpr int REGS_LAUNCH = 168, REGS_CTRL = 56, REGS_SOFT = 224;
+    static_assert(!REGSPLIT || 4 * NWG * REGS_SOFT + 4 * REGS_CTRL == NUM_WARPS * REGS_LAUNCH,
+                  "register split must use exactly the launch pool");
     // ROW_IN_REGS: the softmax holds a whole 128-key S row in registers (one TMEM
-    // round trip per tile); only the single mode has the registers for it.
-    static constexpr bool ROW_IN_REGS = !PAIR;
+    // round trip per tile): the single mode, and the register-split mode.
+    static constexpr bool ROW_IN_REGS = !PAIR || REGSPLIT;
     // TMEM columns of S buffer b, of P buffer b and of the O accumulator of lane w.
     // Without SEP, P (16-bit pairs) occupies the upper BN/2 columns of its S.
     __device__ static constexpr uint32_t s_col(int b) { return static_cast<uint32_t>(b) * 128u; }
@@ -232,8 +244,8 @@ struct Ctl {
     unsigned int *status;
 };
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site,
-                                       bool honour_abort) {
+__device__ __forceinline__ bool wait_slow_body(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site,
+                                               bool honour_abort) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -248,9 +260,27 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl 
     }
 }
 
+// The slow path of a bounded wait as a call (keeps the callers' code small)
+// or inlined (INL: a kernel that moves registers between warpgroups cannot make
+// calls, which would cross code regions whose register counts differ).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site,
+                                       bool honour_abort) {
+    return wait_slow_body(bar, parity, c, site, honour_abort);
+}
+
+template <bool INL>
+__device__ __forceinline__ bool wait_slow_t(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site,
+                                            bool honour_abort) {
+    if constexpr (INL)
+        return wait_slow_body(bar, parity, c, site, honour_abort);
+    else
+        return wait_slow(bar, parity, c, site, honour_abort);
+}
+
+template <bool INL = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c, unsigned site) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, c, site, true);
+    return wait_slow_t<INL>(bar, parity, c, site, true);
 }
 
 // wait sites (recorded in the status word on a timeout)
@@ -345,15 +375,14 @@ __device__ __forceinline__ void exp_half(const uint32_t (&v)[64], int base, int 
 
 // p = exp2(s * sc - m) for a 32-key chunk (keys base..base+31 of the tile):
 // packed fma, MUFU ex2, packed partial sums into acc[4], rounding to 16-bit
-// pairs and one 16-column TMEM store at `dst`.  The packed fp32x2 builtins
-// let the compiler keep operand pairs in register pairs; the element-wise mask
-// exists only in the masked instantiation, which is chosen once per tile.
+// pairs in pk.  The packed fp32x2 builtins let the compiler keep operand pairs
+// in register pairs; the element-wise mask exists only in the masked
+// instantiation, which is chosen once per tile.
 template <bool BF16, bool MASKED>
-__device__ __forceinline__ void exp_chunk(const uint32_t *v, int base, int rel_lo, int rel_hi,
-                                          float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+__device__ __forceinline__ void exp_pack16(const uint32_t *v, int base, int rel_lo, int rel_hi, float sc,
+                                           float neg_m, float2 (&acc)[4], uint32_t (&pk)[16]) {
     const float2 sc2 = make_float2(sc, sc);
     const float2 nm2 = make_float2(neg_m, neg_m);
-    uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
         const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
@@ -368,17 +397,15 @@ __device__ __forceinline__ void exp_chunk(const uint32_t *v, int base, int rel_l
         acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
         pk[e] = pack2<BF16>(pp.x, pp.y);
     }
-    tmem_st16(dst, pk);
 }
 
-// exp_chunk for P in float8 e5m2 (the FP8 P.V variant): the 32 keys are
-// rounded four to a word and stored as 8 TMEM columns at `dst`.
+// The same with P rounded to float8 e5m2 (the FP8 P.V variant): the 32 keys
+// four to a word in pk[8].
 template <bool MASKED>
-__device__ __forceinline__ void exp_chunk8(const uint32_t *v, int base, int rel_lo, int rel_hi,
-                                           float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+__device__ __forceinline__ void exp_pack8q(const uint32_t *v, int base, int rel_lo, int rel_hi, float sc,
+                                           float neg_m, float2 (&acc)[4], uint32_t (&pk)[8]) {
     const float2 sc2 = make_float2(sc, sc);
     const float2 nm2 = make_float2(neg_m, neg_m);
-    uint32_t pk[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         float4 pp;
@@ -402,6 +429,23 @@ __device__ __forceinline__ void exp_chunk8(const uint32_t *v, int base, int rel_
         acc[(2 * e + 1) & 3] = __fadd2_rn(acc[(2 * e + 1) & 3], make_float2(pp.z, pp.w));
         pk[e] = pack4_e5m2(pp.x, pp.y, pp.z, pp.w);
     }
+}
+
+// exp_pack16 followed by one 16-column TMEM store of the pairs at `dst`.
+template <bool BF16, bool MASKED>
+__device__ __forceinline__ void exp_chunk(const uint32_t *v, int base, int rel_lo, int rel_hi,
+                                          float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+    uint32_t pk[16];
+    exp_pack16<BF16, MASKED>(v, base, rel_lo, rel_hi, sc, neg_m, acc, pk);
+    tmem_st16(dst, pk);
+}
+
+// exp_pack8q followed by one 8-column TMEM store of the e5m2 words at `dst`.
+template <bool MASKED>
+__device__ __forceinline__ void exp_chunk8(const uint32_t *v, int base, int rel_lo, int rel_hi,
+                                           float sc, float neg_m, float2 (&acc)[4], uint32_t dst) {
+    uint32_t pk[8];
+    exp_pack8q<MASKED>(v, base, rel_lo, rel_hi, sc, neg_m, acc, pk);
     tmem_st8(dst, pk);
 }
 
@@ -430,41 +474,16 @@ __device__ __forceinline__ void exp_half_any(const uint32_t (&v)[64], int base, 
     }
 }
 
-// exp_chunk without the mask and without the store: the 16 packed pairs stay
-// in `pk` for the caller to store later.
+// Unmasked packs of 32 keys for a later store (16-bit pairs, or e5m2 quads).
 template <bool BF16>
 __device__ __forceinline__ void exp_pack(const uint32_t *v, float sc, float neg_m, float2 (&acc)[4],
                                          uint32_t (&pk)[16]) {
-    const float2 sc2 = make_float2(sc, sc);
-    const float2 nm2 = make_float2(neg_m, neg_m);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
-                                    sc2, nm2);
-        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
-        pk[e] = pack2<BF16>(pp.x, pp.y);
-    }
+    exp_pack16<BF16, false>(v, 0, 0, 0, sc, neg_m, acc, pk);
 }
 
-// exp_pack for P in float8 e5m2: the 32 keys at v packed four to a word into
-// pk, for a later 8-column TMEM store.
 __device__ __forceinline__ void exp_pack8(const uint32_t *v, float sc, float neg_m, float2 (&acc)[4],
                                           uint32_t (&pk)[8]) {
-    const float2 sc2 = make_float2(sc, sc);
-    const float2 nm2 = make_float2(neg_m, neg_m);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1])),
-                                     sc2, nm2);
-        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])),
-                                     sc2, nm2);
-        const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-        const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-        acc[(2 * e) & 3] = __fadd2_rn(acc[(2 * e) & 3], p0);
-        acc[(2 * e + 1) & 3] = __fadd2_rn(acc[(2 * e + 1) & 3], p1);
-        pk[e] = pack4_e5m2(p0.x, p0.y, p1.x, p1.y);
-    }
+    exp_pack8q<false>(v, 0, 0, 0, sc, neg_m, acc, pk);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -474,11 +493,12 @@ __device__ __forceinline__ void exp_pack8(const uint32_t *v, float sc, float neg
 // kind::f8f6f4 MMA; the reference max is the exact running max (threshold 0),
 // so P is rounded against the same max as the page's recurrence.
 template <int D, bool BF16, bool PAIR, bool FP8V = false>
-__global__ void __launch_bounds__(Cfg<D, PAIR>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D, PAIR, FP8V>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
-    using C = Cfg<D, PAIR>;
+    using C = Cfg<D, PAIR, FP8V>;
     constexpr float kThr = FP8V ? 0.f : kRescaleLog2;      // rescale threshold (log2 units)
+    constexpr bool kRowRegs = C::ROW_IN_REGS;
     // V^T rows per ring entry (FP8V) and the bytes of such an entry
     constexpr int V8_ROWS = D / C::EPT;
     constexpr int V8_BYTES = V8_ROWS * BN;
@@ -544,11 +564,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // Waits in every role are polled by all 32 lanes and their outcome made
     // warp-uniform, so warp-collective instructions after them never diverge.
     auto wait_warp = [&](uint32_t bar_addr, uint32_t parity, unsigned site) -> bool {
-        const bool r = wait_bar(bar_addr, parity, ctl, site);
+        const bool r = wait_bar<C::REGSPLIT>(bar_addr, parity, ctl, site);
         return __all_sync(0xffffffffu, r);
     };
 
     const int rounds = tmem_ok ? rounds_all : 0;
+
 
     // MMA issue helpers (called by a whole converged warp; one elected lane issues)
         constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
@@ -592,6 +613,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             }
         };
 
+    // Roles by warpgroup first: with REGSPLIT the copy/MMA warpgroup gives
+    // registers to the softmax warpgroups, each warpgroup executing one
+    // setmaxnreg (the instruction is warpgroup-collective), and the two register
+    // counts never meet in shared code before the end of the kernel.
+    if (warp >= 4 * C::NWG) {
+    if constexpr (C::REGSPLIT) regs_dec<C::REGS_CTRL>();
     if (warp == C::WARP_TMA) {
         // ================================================================ TMA producer
         // (the whole warp runs this loop; one elected lane issues each copy)
@@ -679,10 +706,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // CTA's shared memory goes away.
                 const uint32_t first = rc > static_cast<uint32_t>(C::RING) ? rc - C::RING : 0u;
                 for (uint32_t i = first; i < rc; ++i)
-                    wait_slow(bar(C::B_KVFULL + i % C::RING), (i / C::RING) & 1u, ctl, kSiteDrain, false);
+                    wait_slow_t<C::REGSPLIT>(bar(C::B_KVFULL + i % C::RING), (i / C::RING) & 1u, ctl, kSiteDrain, false);
                 for (int q = 0; q < 4; ++q)
                     if ((qused >> q) & 1u)   // the latest load of slot q has parity !bit
-                        wait_slow(bar(C::B_QFULL + q), ((qpar >> q) & 1u) ^ 1u, ctl, kSiteDrain, false);
+                        wait_slow_t<C::REGSPLIT>(bar(C::B_QFULL + q), ((qpar >> q) & 1u) ^ 1u, ctl, kSiteDrain, false);
             }
         }
         __syncwarp();
@@ -875,7 +902,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             // Every MMA (and the barrier arrivals its commits make) must be done
             // before the CTA frees its tensor memory and exits.
             mma_commit(bar(C::B_DRAIN));
-            wait_slow(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
+            wait_slow_t<C::REGSPLIT>(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
         }
         __syncwarp();
     } else if (C::SEP && warp == C::WARP_PV) {
@@ -917,11 +944,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
             }
             mma_commit(bar(C::B_DRAIN));
-            wait_slow(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
+            wait_slow_t<C::REGSPLIT>(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
         }
         __syncwarp();
+    }
+    // (REGSPLIT: the fourth warp of the copy/MMA warpgroup has no role)
     } else {
         // ================================================================ softmax groups
+        if constexpr (C::REGSPLIT) regs_inc<C::REGS_SOFT>();
         const int wg = warp >> 2;                       // lane (query tile slot) of this group
         const int wq = warp & 3;                        // TMEM lane quarter of this warp
         const int row = wq * 32 + lane;                 // query row inside the tile
@@ -981,7 +1011,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 float alpha = 1.f;
                 bool rescale = false;
                 float neg_m = 0.f;
-                if constexpr (C::ROW_IN_REGS) {
+                if constexpr (kRowRegs) {
                     // Pass 1: the whole S row into registers (one TMEM round trip), then
                     // its extreme (max for sm_scale >= 0, else min).
                     uint32_t sv[BN];
@@ -1010,25 +1040,55 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     }
                     neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
                     if constexpr (C::SEP) {
-                        // P and O of this lane are still read/written by the previous
-                        // tile's P.V until it completes.
+                        // The whole row's P into registers first: the P columns (and O)
+                        // of this lane are still read (written) by the previous tile's
+                        // P.V until it completes, which is waited for only before the
+                        // stores.  (FP8V: e5m2 words, four keys each.)
+                        constexpr int PW = FP8V ? 8 : 16;      // words per 32 keys
+                        uint32_t pk[BN / 32][PW];
+                        if (masked) {
+#pragma unroll
+                            for (int c = 0; c < BN / 32; ++c) {
+                                if constexpr (FP8V)
+                                    exp_pack8q<true>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, pk[c]);
+                                else
+                                    exp_pack16<BF16, true>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, pk[c]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < BN / 32; ++c) {
+                                if constexpr (FP8V)
+                                    exp_pack8q<false>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, pk[c]);
+                                else
+                                    exp_pack16<BF16, false>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, pk[c]);
+                            }
+                        }
                         if (t > 0) {
                             ok = wait_pv(wg);
                             if (!ok) break;
                             tc_fence_after();
                         }
-                    }
-                    // Pass 2: P = exp2(s*scale - m) in 32-key chunks, rounded to 16-bit
-                    // pairs and written to the P columns (without SEP: the upper half
-                    // of this S, whose values are already in registers).
-                    if (masked) {
 #pragma unroll
-                        for (int c = 0; c < BN / 32; ++c)
-                            exp_chunk_any<BF16, true, FP8V>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                        for (int c = 0; c < BN / 32; ++c) {
+                            if constexpr (FP8V)
+                                tmem_st8(p8_addr + 8 * c, pk[c]);
+                            else
+                                tmem_st16(p_addr + 16 * c, pk[c]);
+                        }
                     } else {
+                        // Pass 2: P = exp2(s*scale - m) in 32-key chunks, rounded and
+                        // written over the upper half of this S (whose values are
+                        // already in registers); the previous tile's P.V used the other
+                        // S buffer.
+                        if (masked) {
 #pragma unroll
-                        for (int c = 0; c < BN / 32; ++c)
-                            exp_chunk_any<BF16, false, FP8V>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                            for (int c = 0; c < BN / 32; ++c)
+                                exp_chunk_any<BF16, true, FP8V>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < BN / 32; ++c)
+                                exp_chunk_any<BF16, false, FP8V>(sv + 32 * c, 32 * c, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                        }
                     }
                 } else {
                     bool done = false;

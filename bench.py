@@ -58,6 +58,10 @@ def parse_args():
     ap.add_argument("--threads", type=int, default=None,
                     help="host threads of the CPU oracle (--impl reference and the CPU baseline; "
                          "default: every core)")
+    ap.add_argument("--shape", default=None,
+                    help="an ad hoc problem B,H,L,D,MASK,DTYPE[,BS] (MASK dense|causal|block_diag, "
+                         "DTYPE fp16|bf16) in place of --workload, same input recipe (seed 42, N(0,1)); "
+                         "for profiler runs on reduced sizes")
     ap.add_argument("--lean", action="store_true",
                     help="only the device-timed line: no soak, e2e, CPU baseline or other "
                          "workloads (for profiler runs)")
@@ -414,7 +418,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload] if args.shape is None else shape_workload(args.shape)
 
     if args.impl == "reference":
         if rank != 0:
@@ -538,6 +542,21 @@ def main():
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def shape_workload(spec: str):
+    """A workload from "B,H,L,D,MASK,DTYPE[,BS]" (sm_scale 1/sqrt(D), seed 42, N(0, 1))."""
+    from attn_inputs import Workload
+    f = spec.split(",")
+    if len(f) not in (6, 7):
+        raise SystemExit("--shape wants B,H,L,D,MASK,DTYPE[,BS]")
+    masks = {v: k for k, v in MASK_NAMES.items()}
+    B, H, L, D = (int(x) for x in f[:4])
+    mask = masks[f[4]]
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[f[5]]
+    bs = int(f[6]) if len(f) == 7 else 0
+    return Workload(f"{f[4]}_b{B}h{H}l{L}d{D}_{f[5]}" + (f"_bs{bs}" if bs else ""), B, H, L, D, mask, dt,
+                    1.0 / math.sqrt(D), bs)
 
 
 def attended_pairs(w) -> float:
