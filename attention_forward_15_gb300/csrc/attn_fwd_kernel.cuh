@@ -498,7 +498,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
     using C = Cfg<D, PAIR, FP8V>;
     constexpr float kThr = FP8V ? 0.f : kRescaleLog2;      // rescale threshold (log2 units)
-    constexpr bool kRowRegs = C::ROW_IN_REGS;
     // V^T rows per ring entry (FP8V) and the bytes of such an entry
     constexpr int V8_ROWS = D / C::EPT;
     constexpr int V8_BYTES = V8_ROWS * BN;
@@ -569,7 +568,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     };
 
     const int rounds = tmem_ok ? rounds_all : 0;
-
 
     // MMA issue helpers (called by a whole converged warp; one elected lane issues)
         constexpr uint32_t IDESC_S = idesc_f16_f32acc(BF16, BM, BN, false);
@@ -706,10 +704,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // CTA's shared memory goes away.
                 const uint32_t first = rc > static_cast<uint32_t>(C::RING) ? rc - C::RING : 0u;
                 for (uint32_t i = first; i < rc; ++i)
-                    wait_slow_t<C::REGSPLIT>(bar(C::B_KVFULL + i % C::RING), (i / C::RING) & 1u, ctl, kSiteDrain, false);
+                    wait_slow_t<C::REGSPLIT>(bar(C::B_KVFULL + i % C::RING), (i / C::RING) & 1u, ctl,
+                                             kSiteDrain, false);
                 for (int q = 0; q < 4; ++q)
                     if ((qused >> q) & 1u)   // the latest load of slot q has parity !bit
-                        wait_slow_t<C::REGSPLIT>(bar(C::B_QFULL + q), ((qpar >> q) & 1u) ^ 1u, ctl, kSiteDrain, false);
+                        wait_slow_t<C::REGSPLIT>(bar(C::B_QFULL + q), ((qpar >> q) & 1u) ^ 1u, ctl,
+                                                 kSiteDrain, false);
             }
         }
         __syncwarp();
@@ -947,8 +947,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             wait_slow_t<C::REGSPLIT>(bar(C::B_DRAIN), 0, ctl, kSiteDrain, false);
         }
         __syncwarp();
-    }
-    // (REGSPLIT: the fourth warp of the copy/MMA warpgroup has no role)
+    }  // (REGSPLIT: the fourth warp of the copy/MMA warpgroup has no role)
     } else {
         // ================================================================ softmax groups
         if constexpr (C::REGSPLIT) regs_inc<C::REGS_SOFT>();
@@ -1011,7 +1010,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 float alpha = 1.f;
                 bool rescale = false;
                 float neg_m = 0.f;
-                if constexpr (kRowRegs) {
+                if constexpr (C::ROW_IN_REGS) {
                     // Pass 1: the whole S row into registers (one TMEM round trip), then
                     // its extreme (max for sm_scale >= 0, else min).
                     uint32_t sv[BN];
