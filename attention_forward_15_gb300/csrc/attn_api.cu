@@ -25,7 +25,7 @@ struct DeviceState {
     int sms = 0;
     unsigned int *status = nullptr;   // device status word written by timed-out waits
     bool smem_attr[6][2] = {};        // per (kernel, dtype): dynamic smem attribute set
-    bool bwd_attr[2][2][2] = {};      // backward: per (head dim, dtype, dK/dV | dQ)
+    bool bwd_attr[3][2][2] = {};      // backward: per (head dim, dtype, dK/dV | dQ)
 };
 
 std::mutex g_mutex;
@@ -134,13 +134,14 @@ int device_state(DeviceState **out, int *dev_out) {
 }
 
 // 3-D tensor map over a [BH, L, D] 16-bit array: box = 64 columns (128 bytes)
-// x 128 rows x 1 head, 128-byte swizzle; rows past L read as zero.
-int encode_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype) {
+// x `rows` rows (128, or 64 for the half-tile ring entries of the D = 256
+// backward) x 1 head, 128-byte swizzle; rows past L read as zero.
+int encode_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype, int rows = 128) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                              static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -556,7 +557,7 @@ int launch_bwd(DeviceState &st, const CUtensorMap &f0, const CUtensorMap &f1, co
     auto kern = attn::attn_bwd_kernel<D, BF16, DQ>;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
-        bool &set = st.bwd_attr[D == 64 ? 0 : 1][BF16 ? 1 : 0][DQ ? 1 : 0];
+        bool &set = st.bwd_attr[D == 64 ? 0 : (D == 128 ? 1 : 2)][BF16 ? 1 : 0][DQ ? 1 : 0];
         if (!set) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
                 cudaSuccess)
@@ -565,7 +566,8 @@ int launch_bwd(DeviceState &st, const CUtensorMap &f0, const CUtensorMap &f1, co
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(prm.BH) * static_cast<unsigned>(prm.n_t));
+    // one CTA per (head, fixed tile); DSPLIT: two, one per head-dim half
+    cfg.gridDim = dim3(static_cast<unsigned>(prm.BH) * static_cast<unsigned>(prm.n_t) * (C::DSPLIT ? 2u : 1u));
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
@@ -581,18 +583,22 @@ int launch_bwd(DeviceState &st, const CUtensorMap &f0, const CUtensorMap &f1, co
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// t*: maps with 128-row boxes (fixed tiles, and streamed ones of a whole-tile
+// ring); s*: the streamed operands' maps (64-row boxes when the ring holds
+// half tiles, D = 256).
 template <int D, bool BF16>
 int bwd_for_dim(DeviceState &st, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                const CUtensorMap &tg, attn::BwdParams prm, void *dq, void *dk, void *dv, cudaStream_t s) {
+                const CUtensorMap &tg, const CUtensorMap &sq, const CUtensorMap &sk, const CUtensorMap &sv,
+                const CUtensorMap &sg, attn::BwdParams prm, void *dq, void *dk, void *dv, cudaStream_t s) {
     // dK/dV: fixed K, V; streamed Q, dO
     prm.g0 = dk;
     prm.g1 = dv;
-    int rc = launch_bwd<D, BF16, false>(st, tk, tv, tq, tg, prm, s);
+    int rc = launch_bwd<D, BF16, false>(st, tk, tv, sq, sg, prm, s);
     if (rc != ATTN_OK) return rc;
     // dQ: fixed Q, dO; streamed K, V
     prm.g0 = dq;
     prm.g1 = nullptr;
-    return launch_bwd<D, BF16, true>(st, tq, tg, tk, tv, prm, s);
+    return launch_bwd<D, BF16, true>(st, tq, tg, sk, sv, prm, s);
 }
 
 }  // namespace
@@ -610,7 +616,6 @@ int attn_bwd_check(const void *q, const void *k, const void *v, const void *o, c
                    float sm_scale, int dtype) {
     int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
     if (rc != ATTN_OK) return rc;
-    if (D > 128) return ATTN_ERR_UNSUPPORTED;
     if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
     if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
@@ -683,17 +688,26 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     if (rc == ATTN_OK) rc = encode_map(&tg, dout, prm.BH, L, D, dtype);
     if (rc != ATTN_OK) return rc;
     if (kernel_dim(D) == 64)
-        return bf16 ? bwd_for_dim<64, true>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s)
-                    : bwd_for_dim<64, false>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s);
-    return bf16 ? bwd_for_dim<128, true>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s)
-                : bwd_for_dim<128, false>(*st, tq, tk, tv, tg, prm, dq, dk, dv, s);
+        return bf16 ? bwd_for_dim<64, true>(*st, tq, tk, tv, tg, tq, tk, tv, tg, prm, dq, dk, dv, s)
+                    : bwd_for_dim<64, false>(*st, tq, tk, tv, tg, tq, tk, tv, tg, prm, dq, dk, dv, s);
+    if (kernel_dim(D) == 128)
+        return bf16 ? bwd_for_dim<128, true>(*st, tq, tk, tv, tg, tq, tk, tv, tg, prm, dq, dk, dv, s)
+                    : bwd_for_dim<128, false>(*st, tq, tk, tv, tg, tq, tk, tv, tg, prm, dq, dk, dv, s);
+    // D = 256: the streamed operands travel as 64-row halves
+    CUtensorMap sq, sk, sv, sg;
+    rc = encode_map(&sq, q, prm.BH, L, D, dtype, 64);
+    if (rc == ATTN_OK) rc = encode_map(&sk, k, prm.BH, L, D, dtype, 64);
+    if (rc == ATTN_OK) rc = encode_map(&sv, v, prm.BH, L, D, dtype, 64);
+    if (rc == ATTN_OK) rc = encode_map(&sg, dout, prm.BH, L, D, dtype, 64);
+    if (rc != ATTN_OK) return rc;
+    return bf16 ? bwd_for_dim<256, true>(*st, tq, tk, tv, tg, sq, sk, sv, sg, prm, dq, dk, dv, s)
+                : bwd_for_dim<256, false>(*st, tq, tk, tv, tg, sq, sk, sv, sg, prm, dq, dk, dv, s);
 }
 
 int attn_bwd_work(int B, int H, int L, int D, int mask_kind, int block_size, int dtype, double *flops,
                   double *bytes) {
     int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
     if (rc != ATTN_OK) return rc;
-    if (D > 128) return ATTN_ERR_UNSUPPORTED;
     double f = 0.0;
     rc = attn_fwd_work(B, H, L, D, mask_kind, block_size, dtype, &f, nullptr);
     if (rc != ATTN_OK) return rc;

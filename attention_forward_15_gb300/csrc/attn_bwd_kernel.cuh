@@ -36,7 +36,10 @@
 // P (16-bit pairs) over the first 16 of its S columns and its dS over the
 // first 16 of its dP columns, once read; a half's next S and dP
 // are issued after the products that read its P and dS, on the same in-order
-// MMA pipe.  D is 64 or 128 (256 + 2D columns).
+// MMA pipe.  D is 64 or 128 (256 + 2D columns), or 256: then the fixed pair
+// fills 128 KB of shared memory, the ring holds one 64-row half of the streamed
+// pair at a time, and dK/dV runs two CTAs per key tile, each accumulating one
+// half of the head dim (256 + 2 x 128 columns; dQ: 256 + 256).
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -111,17 +114,29 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
 template <int D, bool DQ>
 struct BwdCfg {
     static constexpr int CHUNKS = D / 64;               // 128-byte-wide TMA boxes per row
-    static constexpr int CHUNK_BYTES = 128 * 128;
+    static constexpr int CHUNK_BYTES = 128 * 128;       // one box of a fixed tile: 128 rows
     static constexpr int TILE_BYTES = 128 * D * 2;
-    static constexpr int NS = D == 64 ? 3 : 2;          // ring stages of streamed pairs
+    // D = 256: the fixed pair alone takes 128 KB of shared memory, so the ring
+    // holds the 64-row halves of the streamed tiles (one stage of the two
+    // operands, 64 KB) instead of whole tiles.
+    static constexpr bool HALF_RING = D == 256;
+    static constexpr int RCHUNK_BYTES = HALF_RING ? 64 * 128 : CHUNK_BYTES;  // one box of a ring operand
+    static constexpr int RTILE_BYTES = HALF_RING ? TILE_BYTES / 2 : TILE_BYTES;
+    static constexpr int NS = HALF_RING ? 1 : (D == 64 ? 3 : 2);   // ring stages of streamed pairs
+    // dK/dV at D = 256: the two accumulators would need 2 x 256 columns of tensor
+    // memory next to S and dP, so each CTA keeps half of the head dim of dK and
+    // dV (two CTAs per key tile, both computing S and dP over the whole head dim)
+    static constexpr bool DSPLIT = HALF_RING && !DQ;
+    static constexpr int DA = DSPLIT ? D / 2 : D;        // accumulator width (columns)
     // four compute warpgroups (group w takes 32 of the 64 rows of half w/2 of
     // every streamed tile), a TMA warp and an MMA warp
     static constexpr int THREADS = 576;
     static constexpr int WARP_TMA = 16, WARP_MMA = 17;
-    static constexpr int VEC_BYTES = DQ ? 0 : 2 * 128 * 4;   // -lse2 and -Di of one query tile
+    static constexpr int VEC_ROWS = HALF_RING ? 64 : 128;    // rows of a ring entry
+    static constexpr int VEC_BYTES = DQ ? 0 : 2 * VEC_ROWS * 4;   // -lse2 and -Di of those rows
     static constexpr int OFF_FIX = 0;                        // F0 | F1
     static constexpr int OFF_RING = 2 * TILE_BYTES;          // NS x (R0 | R1)
-    static constexpr int OFF_VEC = OFF_RING + NS * 2 * TILE_BYTES;
+    static constexpr int OFF_VEC = OFF_RING + NS * 2 * RTILE_BYTES;
     static constexpr int OFF_BAR = OFF_VEC + NS * VEC_BYTES;
     static constexpr int B_FIX = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_SFULL = 1 + 2 * NS;   // SFULL, PFULL: one per half
     static constexpr int B_PFULL = B_SFULL + 2, B_DONE = B_PFULL + 2, B_DRAIN = B_DONE + 1;
@@ -131,9 +146,11 @@ struct BwdCfg {
     static constexpr int HALF_BYTES = 64 * 128;          // 64 rows of a 128-byte-wide box
     __device__ static constexpr uint32_t col_s(int h) { return 128u * static_cast<uint32_t>(h); }
     __device__ static constexpr uint32_t col_dp(int h) { return 128u * static_cast<uint32_t>(h) + 64u; }
-    static constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = 256 + D;
+    // ACC0 (dV, dK/dV only) and ACC1 (dK or dQ) after the S and dP buffers
+    static constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = DQ ? 256 : 256 + DA;
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(D == 64 || D == 128, "backward head dim");
+    static_assert(D == 64 || D == 128 || D == 256, "backward head dim");
+    static_assert(COL_ACC1 + DA <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -161,12 +178,12 @@ __device__ __forceinline__ void bwd_range(const BwdParams &p, bool dq, int f, in
 // dS (and P) of one chunk of NE columns: rows are this thread's TMEM lane,
 // columns c0..c0+NE-1 of the tile.  S, dP: fp32 raw scores and dP of the chunk.  The
 // negated lse2 and Di come per row (dQ: nl_row, nd_row) or per column (dK/dV:
-// the shared-memory vectors, read four at a time); packed fp32x2 arithmetic as
-// in the forward; `keep` masks (row, column).
+// the shared-memory vectors from entry vc0 on, read four at a time); packed
+// fp32x2 arithmetic as in the forward; `keep` masks (row, column).
 template <bool BF16, bool DQ, bool MASKED, int NE>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&S)[NE], const uint32_t (&dP)[NE], float sc,
                                           float nl_row, float nd_row, const float *col_nl,
-                                          const float *col_nd, int c0, int mask, int bs, int L,
+                                          const float *col_nd, int c0, int vc0, int mask, int bs, int L,
                                           int row_idx, int col_base, uint32_t (&pk)[NE / 2],
                                           uint32_t (&dk)[NE / 2]) {
     static_assert(NE % 4 == 0, "bwd_chunk: whole float4s of the column vectors");
@@ -178,8 +195,8 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&S)[NE], const uint32_
             nl = make_float2(nl_row, nl_row);
             nd = make_float2(nd_row, nd_row);
         } else {
-            const float4 a = reinterpret_cast<const float4 *>(col_nl + c0)[e >> 1];
-            const float4 b = reinterpret_cast<const float4 *>(col_nd + c0)[e >> 1];
+            const float4 a = reinterpret_cast<const float4 *>(col_nl + vc0)[e >> 1];
+            const float4 b = reinterpret_cast<const float4 *>(col_nd + vc0)[e >> 1];
             nl = (e & 1) ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
             nd = (e & 1) ? make_float2(b.z, b.w) : make_float2(b.x, b.y);
         }
@@ -229,11 +246,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
     // unit of this CTA: (head, fixed tile).  Causal: heaviest fixed tiles first
     // across all heads; otherwise head-major, so that CTAs running together
     // stream the same head's tiles (shared in L2)
+    // (DSPLIT: the two CTAs of a key tile are neighbours; dc = head-dim half)
+    const unsigned bid = C::DSPLIT ? blockIdx.x >> 1 : blockIdx.x;
+    const int dc = C::DSPLIT ? static_cast<int>(blockIdx.x & 1u) : 0;
     const bool head_major = p.mask != kMaskCausal;
-    const int bh = head_major ? static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_t))
-                              : static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
-    const int rank = head_major ? static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_t))
-                                : static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));
+    const int bh = head_major ? static_cast<int>(bid / static_cast<unsigned>(p.n_t))
+                              : static_cast<int>(bid % static_cast<unsigned>(p.BH));
+    const int rank = head_major ? static_cast<int>(bid % static_cast<unsigned>(p.n_t))
+                                : static_cast<int>(bid / static_cast<unsigned>(p.BH));
     const int f = (p.mask == kMaskCausal && DQ) ? p.n_t - 1 - rank : rank;
     int lo, hi;
     bwd_range(p, DQ, f, lo, hi);
@@ -293,23 +313,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             }
             fix_issued = true;
         }
-        for (int t = 0; t < nn && ok; ++t) {
-            const int s = t % C::NS;
-            ok = wait_warp(bar(C::B_EMPTY + s), ((t / C::NS) & 1) ^ 1, kSiteKvEmpty);
+        // ring entries: whole streamed tiles, or (HALF_RING) their 64-row halves in turn
+        constexpr int PER_TILE = C::HALF_RING ? 2 : 1;
+        for (int q = 0; q < PER_TILE * nn && ok; ++q) {
+            const int s = q % C::NS;
+            ok = wait_warp(bar(C::B_EMPTY + s), ((q / C::NS) & 1) ^ 1, kSiteKvEmpty);
             if (!ok) break;
-            const int j = lo + t;
-            mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE_BYTES + C::VEC_BYTES);
-            const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE_BYTES;
+            const int j = lo + q / PER_TILE;
+            const int row0 = j * 128 + (q % PER_TILE) * 64;
+            mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::RTILE_BYTES + C::VEC_BYTES);
+            const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::RTILE_BYTES;
             for (int c = 0; c < C::CHUNKS; ++c) {
-                tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_r0, c * 64, j * 128, bh, bar(C::B_FULL + s));
-                tma_load_3d(dst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_r1, c * 64, j * 128, bh,
+                tma_load_3d(dst + c * C::RCHUNK_BYTES, &tm_r0, c * 64, row0, bh, bar(C::B_FULL + s));
+                tma_load_3d(dst + C::RTILE_BYTES + c * C::RCHUNK_BYTES, &tm_r1, c * 64, row0, bh,
                             bar(C::B_FULL + s));
             }
             if constexpr (!DQ) {
-                const size_t off = static_cast<size_t>(bh) * p.n_pad + static_cast<size_t>(j) * 128;
+                const size_t off = static_cast<size_t>(bh) * p.n_pad + static_cast<size_t>(row0);
                 const uint32_t vdst = s_base + C::OFF_VEC + s * C::VEC_BYTES;
-                bulk_load_1d(vdst, p.nlse2 + off, 512, bar(C::B_FULL + s));
-                bulk_load_1d(vdst + 512, p.ndelta + off, 512, bar(C::B_FULL + s));
+                bulk_load_1d(vdst, p.nlse2 + off, C::VEC_ROWS * 4, bar(C::B_FULL + s));
+                bulk_load_1d(vdst + C::VEC_ROWS * 4, p.ndelta + off, C::VEC_ROWS * 4, bar(C::B_FULL + s));
             }
             ++issued;
         }
@@ -324,23 +347,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
     } else if (warp == C::WARP_MMA) {
         // ================================================================ MMA issuer
         constexpr uint32_t IDESC_SS = idesc_f16_f32acc(BF16, 128, 64, false);
-        constexpr uint32_t IDESC_ACC = idesc_f16_f32acc(BF16, 128, D, true);
+        constexpr uint32_t IDESC_ACC = idesc_f16_f32acc(BF16, 128, C::DA, true);
         const uint32_t f0 = s_base + C::OFF_FIX, f1 = f0 + C::TILE_BYTES;
         // X = A B^T over the head dim for 64 rows of B: both K-major, k-step kk
-        // = head-dim columns [16kk, 16kk+16): box kk/4, 32-byte offset kk%4.
+        // = head-dim columns [16kk, 16kk+16): box kk/4 (fixed A: CHUNK_BYTES apart,
+        // ring B: RCHUNK_BYTES apart), 32-byte offset kk%4.
         auto issue_ss = [&](uint32_t a, uint32_t b, uint32_t dcol) {
             const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
-                mma_ss(tmem + dcol, ad + off, bd + off, IDESC_SS, kk > 0 ? 1u : 0u);
+                const uint64_t aoff = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
+                const uint64_t boff = (kk >> 2) * (C::RCHUNK_BYTES >> 4) + (kk & 3) * 2;
+                mma_ss(tmem + dcol, ad + aoff, bd + boff, IDESC_SS, kk > 0 ? 1u : 0u);
             }
         };
         // ACC += A(TMEM, 16-bit pairs) B over 64 rows of B, B MN-major: k-step kk
-        // = rows [16kk, 16kk+16); its 64-column boxes are CHUNK_BYTES apart.  The
-        // A pairs of rows [32g, 32g+32) sit at columns 32g..32g+15 of the half.
+        // = rows [16kk, 16kk+16); its 64-column boxes are RCHUNK_BYTES apart (DSPLIT:
+        // starting at the head-dim half dc).  The A pairs of rows [32g, 32g+32)
+        // sit at columns 32g..32g+15 of the half.
         auto issue_acc = [&](uint32_t acol, uint32_t b, uint32_t dcol, bool accumulate) {
-            const uint64_t bd = sdesc_sw128(b, C::CHUNK_BYTES, 1024);
+            const uint64_t bd =
+                sdesc_sw128(b + static_cast<uint32_t>(dc * (C::DA / 64) * C::RCHUNK_BYTES), C::RCHUNK_BYTES, 1024);
 #pragma unroll
             for (int kk = 0; kk < 64 / 16; ++kk)
                 mma_ts(tmem + dcol, tmem + acol + (kk >> 1) * 32 + (kk & 1) * 8,
@@ -355,6 +382,29 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         };
         bool ok = nn > 0;
         if (ok) ok = wait_warp(bar(C::B_FIX), 0, kSiteQFull);
+        if constexpr (C::HALF_RING) {
+            // One ring entry per 64-row half: its S and dP, then (once the half's
+            // compute warps have written P and dS) its two accumulations, which
+            // free the entry for the next half.
+            for (int q = 0; q < 2 * nn && ok; ++q) {
+                const int t = q >> 1, h = q & 1, s = q % C::NS;
+                ok = wait_warp(bar(C::B_FULL + s), (q / C::NS) & 1, kSiteKvFullK);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t r0 = s_base + C::OFF_RING + s * 2 * C::RTILE_BYTES;
+                const uint32_t r1 = r0 + C::RTILE_BYTES;
+                issue_ss(f0, r0, C::col_s(h));
+                issue_ss(f1, r1, C::col_dp(h));
+                mma_commit(bar(C::B_SFULL + h));
+                ok = wait_warp(bar(C::B_PFULL + h), t & 1, kSitePFull);
+                if (!ok) break;
+                tc_fence_after();
+                if constexpr (!DQ) issue_acc(C::col_s(h), r1, C::COL_ACC0, q > 0);   // dV += P^T dO
+                issue_acc(C::col_dp(h), r0, C::COL_ACC1, q > 0);                       // dK += dS^T Q | dQ += dS K
+                mma_commit(bar(C::B_EMPTY + s));
+            }
+            ok = ok && nn > 0;
+        } else {
         if (ok) ok = wait_warp(bar(C::B_FULL + 0), 0, kSiteKvFullK);
         if (ok) {
             tc_fence_after();
@@ -385,6 +435,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
                 }
             }
         }
+        }   // whole-tile ring
         if (ok && nn > 0) mma_commit(bar(C::B_DONE));
         // every MMA (and the arrivals its commits make) done before the CTA
         // frees tensor memory and exits
@@ -411,7 +462,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         const uint32_t cd = tmem + lane_off + C::col_dp(h) + 32 * g;   // and dP columns
         bool ok = true;
         for (int t = 0; t < nn && ok; ++t) {
-            const int s = t % C::NS;
+            // ring entry of this group's half: the tile's (whole-tile ring) or the
+            // half's own (HALF_RING, whose vectors then start at the half's rows)
+            const int s = C::HALF_RING ? (2 * t + h) % C::NS : t % C::NS;
             const int j = lo + t;
             const float *vec = reinterpret_cast<const float *>(smem + C::OFF_VEC + s * C::VEC_BYTES);
             // tiles that cross the mask, and (dQ) a ragged last key tile
@@ -428,12 +481,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
                 tmem_wait_ld();
                 uint32_t pk[8], dk[8];
                 const int c0 = 64 * h + 32 * g + 16 * c;     // column of the sub-chunk in the tile
+                const int vc0 = C::HALF_RING ? c0 - 64 * h : c0;
                 if (masked)
-                    bwd_chunk<BF16, DQ, true, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
-                                                  p.L, row_idx, j * 128, pk, dk);
+                    bwd_chunk<BF16, DQ, true, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + C::VEC_ROWS, c0, vc0,
+                                                  p.mask, p.bs, p.L, row_idx, j * 128, pk, dk);
                 else
-                    bwd_chunk<BF16, DQ, false, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + 128, c0, p.mask, p.bs,
-                                                   p.L, row_idx, j * 128, pk, dk);
+                    bwd_chunk<BF16, DQ, false, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + C::VEC_ROWS, c0, vc0,
+                                                   p.mask, p.bs, p.L, row_idx, j * 128, pk, dk);
                 // P and dS of sub-chunk c to columns [8c, 8c+8) of this group's
                 // S and dP columns, which it has read by now
                 if constexpr (!DQ) tmem_st8(cs + 8 * c, pk);
@@ -449,17 +503,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             tc_fence_after();
             const bool row_valid = row_idx < p.L;
             // 32-column jobs: ACC1 (dK or dQ, times sm_scale) to g0, and (dK/dV)
-            // ACC0 (dV) to g1, dealt round-robin to the four groups
-            constexpr int NJ = (DQ ? 1 : 2) * (D / 32);
+            // ACC0 (dV) to g1, dealt round-robin to the four groups; the
+            // accumulators hold head-dim columns [dc * DA, dc * DA + DA)
+            constexpr int NJ = (DQ ? 1 : 2) * (C::DA / 32);
 #pragma unroll 1
             for (int jb = wg; jb < NJ; jb += 4) {
-                const bool to_g0 = jb < D / 32;
-                const int c = jb % (D / 32);
-                if (32 * c >= p.d_out) continue;
+                const bool to_g0 = jb < C::DA / 32;
+                const int c = jb % (C::DA / 32);
+                const int col0 = dc * C::DA + 32 * c;           // first head-dim column of the job
+                if (col0 >= p.d_out) continue;
                 const uint32_t acol = to_g0 ? C::COL_ACC1 : C::COL_ACC0;
                 const float mul = to_g0 ? p.scale : 1.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(to_g0 ? p.g0 : p.g1) +
-                                                       ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out) * 2);
+                                                       ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out +
+                                                        static_cast<size_t>(dc) * C::DA) * 2);
                 uint32_t raw[32];
                 tmem_ld32(tmem + lane_off + acol + 32 * c, raw);
                 tmem_wait_ld();
@@ -470,7 +527,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
                 if (row_valid) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
-                        if (32 * c + 8 * v4 < p.d_out)
+                        if (col0 + 8 * v4 < p.d_out)
                             dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
                                                          w16[4 * v4 + 3]);
                 }

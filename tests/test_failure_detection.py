@@ -55,13 +55,15 @@ def test_timeout_is_reported_and_recovered(af, D, mask, dt):
     assert af.last_device_status(0)[0] == 0
 
 
-def test_bwd_timeout_is_reported_and_recovered(af):
+@pytest.mark.parametrize("D", [64, 256])
+def test_bwd_timeout_is_reported_and_recovered(af, D):
     """The same for the backward's two tile kernels (one small head, so every
-    CTA's wait runs out at once): the timeout is reported with a wait site, and
-    the next backward on the same context is right."""
+    CTA's wait runs out at once; D = 256 runs the half-tile ring): the timeout
+    is reported with a wait site, and the next backward on the same context is
+    right."""
     lib = af.load_library()
     dev = torch.device("cuda", 0)
-    q, k, v = make_qkv(1, 1, 256, 64, torch.float16, seed=6)
+    q, k, v = make_qkv(1, 1, 256, D, torch.float16, seed=6)
     g = torch.randn(q.shape, generator=torch.Generator().manual_seed(7)).to(q.dtype)
     qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
     o, lse = af.fwd(qd, kd, vd, CAUSAL)
@@ -79,7 +81,7 @@ def test_bwd_timeout_is_reported_and_recovered(af):
     dq, dk, dv = af.bwd(qd, kd, vd, o, lse, gd, CAUSAL)
     torch.cuda.synchronize()
     assert af.last_device_status(0)[0] == 0
-    ref = oracle.attention_bwd(q, k, v, g, CAUSAL, 0, float(np.float32(1.0 / 8.0)), bounds=True)
+    ref = oracle.attention_bwd(q, k, v, g, CAUSAL, 0, float(np.float32(1.0 / math.sqrt(D))), bounds=True)
     u = 2.0 ** -11
     for got, want, bnd in zip((dq, dk, dv), ref[:3], ref[3:]):
         err = np.abs(got.double().cpu().numpy() - want)

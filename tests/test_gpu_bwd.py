@@ -83,6 +83,12 @@ CASES = [
     (1, 2, 512, 64, BLOCK_DIAG, 16, torch.bfloat16),
     (1, 2, 256, 32, CAUSAL, 0, torch.float16),          # padded head dims
     (1, 2, 256, 96, DENSE, 0, torch.bfloat16),
+    (1, 2, 256, 256, DENSE, 0, torch.bfloat16),         # D = 256: half-tile ring, dK/dV split
+    (1, 2, 384, 256, CAUSAL, 0, torch.float16),
+    (1, 2, 512, 256, BLOCK_DIAG, 64, torch.bfloat16),
+    (1, 2, 300, 256, CAUSAL, 0, torch.bfloat16),        # ragged
+    (2, 1, 256, 200, DENSE, 0, torch.float16),          # padded into the 256 kernel
+    (1, 2, 512, 256, BLOCK_DIAG, 256, torch.float16),
 ]
 
 
@@ -114,10 +120,10 @@ def test_bwd_deterministic(af):
 
 def test_bwd_argument_errors(af):
     dev = torch.device("cuda", 0)
-    q = torch.zeros((1, 1, 128, 256), dtype=torch.float16, device=dev)
+    q = torch.zeros((1, 1, 128, 100), dtype=torch.float16, device=dev)
     lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
     with pytest.raises(af.AttnError) as e:
-        af.bwd(q, q, q, q, lse, q)                    # D = 256 has no backward kernel
+        af.bwd(q, q, q, q, lse, q)                    # head dims are multiples of 8
     assert e.value.status == 4
     q = torch.zeros((1, 1, 128, 64), dtype=torch.float16, device=dev)
     lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
@@ -126,13 +132,20 @@ def test_bwd_argument_errors(af):
     assert e.value.status == 8
 
 
-@pytest.mark.parametrize("name", ["causal_b2h32l4096d128_bf16", "dense_b4h16l1024d64_f16"])
+@pytest.mark.parametrize("name", ["causal_b2h32l4096d128_bf16", "dense_b4h16l1024d64_f16",
+                                  "dense_b1h16l2048d256_bf16"])
 def test_bwd_full_size_heads(af, name):
     """The backward of a full-size workload, in one launch sequence as the
-    benchmark runs it; the first and the last head compared element by element
-    with the oracle's gradients of those heads."""
-    from attn_inputs import WORKLOADS
-    w = WORKLOADS[name]
+    benchmark runs it (the D = 256 workload at L = 2048 instead of 16384, so
+    that the oracle's two heads stay within seconds); the first and the last
+    head compared element by element with the oracle's gradients of those
+    heads."""
+    import math as _m
+    from attn_inputs import WORKLOADS, Workload
+    if name == "dense_b1h16l2048d256_bf16":
+        w = Workload(name, 1, 16, 2048, 256, DENSE, torch.bfloat16, 1.0 / _m.sqrt(256))
+    else:
+        w = WORKLOADS[name]
     q, k, v = make_qkv(w.B, w.H, w.L, w.D, w.dtype, seed=w.seed)
     g = _dout(q, 99)
     dev = torch.device("cuda", 0)
