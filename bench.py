@@ -493,10 +493,10 @@ def main():
             fp8_pv[name] = {"mask": MASK_NAMES[ow.mask], "ms": round(ms2, 4),
                             "tflops": round(f2 / (ms2 * 1e-3) / 1e12, 2),
                             "frac_of_bf16_peak": round(f2 / (ms2 * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
-    # The backward (attn_bwd: dQ, dK, dV) on the D <= 128 workloads.
+    # The backward (attn_bwd: dQ, dK, dV) at D = 64, 128 and 256.
     bwd_lines = {}
     if not args.no_all:
-        for name in (w.name, "causal_b2h32l4096d128_bf16"):
+        for name in (w.name, "causal_b2h32l4096d128_bf16", "dense_b1h16l16384d256_bf16"):
             ow = WORKLOADS[name]
             fb, _ = af.bwd_work(ow.B, ow.H, ow.L, ow.D, ow.mask, ow.block_size, ow.dtype)
             msb = time_bwd(af, ow, dev, 40 if ow.L >= 4096 else 100, 3)

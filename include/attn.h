@@ -255,7 +255,8 @@ int attn_debug_inject(int mode);
  *   workspace         device scratch of at least attn_bwd_workspace_size(B, H,
  *                     L) bytes, 16-byte aligned, owned by the caller, free for
  *                     reuse once the call's work on `stream` has completed.
- *   D                 a multiple of 8 from 8 to 128 (kernels for 64 and 128);
+ *   D                 a multiple of 8 from 8 to 256 (kernels for 64, 128 and
+ *                     256; other D run zero-padded to the next of these);
  *                     other arguments as for attn_fwd.
  * Every pointer must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
  *
