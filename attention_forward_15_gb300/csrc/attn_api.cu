@@ -134,8 +134,9 @@ int device_state(DeviceState **out, int *dev_out) {
 }
 
 // 3-D tensor map over a [BH, L, D] 16-bit array: box = 64 columns (128 bytes)
-// x `rows` rows (128, or 64 for the half-tile ring entries of the D = 256
-// backward) x 1 head, 128-byte swizzle; rows past L read as zero.
+// x `rows` rows (128; 64 for the half-tile ring entries of the D = 256
+// backward; 32 for the forward's staged O stores) x 1 head, 128-byte swizzle;
+// rows past L read as zero (and are not written by stores).
 int encode_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype, int rows = 128) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                           static_cast<cuuint64_t>(BH)};
@@ -191,12 +192,14 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
             set = true;
         }
     }
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
+    std::memset(&to, 0, sizeof(to));      // (unused unless O rows are staged)
     int rc = encode_map(&tq, q, prm.BH, prm.L, prm.d_out, dtype);
     if (rc == ATTN_OK) rc = encode_map(&tk, k, prm.BH, prm.L, prm.d_out, dtype);
     if (rc == ATTN_OK)
         rc = FP8V ? encode_map_vt8(&tv, v, prm.BH, prm.L, prm.d_out, D / C::EPT)
                   : encode_map(&tv, v, prm.BH, prm.L, prm.d_out, dtype);
+    if (rc == ATTN_OK && C::OSTAGE) rc = encode_map(&to, prm.o, prm.BH, prm.L, prm.d_out, dtype, 32);
     if (rc != ATTN_OK) return rc;
     const int grid = prm.n_units < st.sms ? prm.n_units : st.sms;
     // Programmatic dependent launch: the CTAs may be scheduled while the
@@ -212,7 +215,7 @@ int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdPara
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, prm) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
     }

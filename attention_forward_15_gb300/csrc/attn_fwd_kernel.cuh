@@ -136,7 +136,13 @@ struct Cfg {
     static constexpr int NQB = D == 64 ? 2 : 1;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQB * NQ * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_RING + RING * ENTRY_BYTES;
+    // OSTAGE (D = 64 separate-P mode): each softmax warp writes its 32 rows of
+    // O through a shared slab of its own with one TMA store.  A thread storing
+    // its own 128-byte row from registers touches 32 lines per instruction.
+    static constexpr bool OSTAGE = SEP;
+    static constexpr int OST_WARP_BYTES = 32 * D * 2;
+    static constexpr int OFF_OST = OFF_RING + RING * ENTRY_BYTES;
+    static constexpr int OFF_BAR = OFF_OST + (OSTAGE ? 4 * NWG * OST_WARP_BYTES : 0);
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = 4, B_KVFULL = 8;
     static constexpr int B_KVEMPTY = B_KVFULL + RING;
@@ -153,6 +159,7 @@ struct Cfg {
     static_assert(PAIR ? (2 * 128 + 2 * D <= 512) : (D == 256), "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(PAIR ? EPT == 1 : true, "pair modes keep whole-tile ring entries");
+    static_assert(!OSTAGE || D == 64, "staged O rows are one 128-byte swizzle row");
 };
 
 // ------------------------------------------------------------ work units
@@ -252,6 +259,7 @@ __device__ __forceinline__ bool wait_slow_body(uint32_t bar, uint32_t parity, co
         if ((it & 63u) == 63u) {
             if (honour_abort && *c.abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                griddep_wait();
                 atomicCAS(c.status, 0u, kStatusTimeout | (site << 8));
                 *c.abort_flag = 1;
                 return false;
@@ -495,7 +503,8 @@ __device__ __forceinline__ void exp_pack8(const uint32_t *v, float sc, float neg
 template <int D, bool BF16, bool PAIR, bool FP8V = false>
 __global__ void __launch_bounds__(Cfg<D, PAIR, FP8V>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+                const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                const FwdParams p) {
     using C = Cfg<D, PAIR, FP8V>;
     constexpr float kThr = FP8V ? 0.f : kRescaleLog2;      // rescale threshold (log2 units)
     // V^T rows per ring entry (FP8V) and the bytes of such an entry
@@ -539,6 +548,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
+        if constexpr (C::OSTAGE) tma_prefetch_desc(&tmap_o);
     }
     if (warp == C::WARP_MMA) {
         tmem_alloc(s_base + C::OFF_MISC, C::TMEM_COLS);
@@ -547,18 +557,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Launched as a programmatic dependent: everything above touches only this
-    // CTA's own resources; global memory may be written by the previous kernel
-    // of the stream until it completes.  Dependents of this kernel may be
-    // scheduled from now on (they wait for its completion in the same way).
-    griddep_wait();
+    // Launched as a programmatic dependent: global memory may be written by the
+    // previous kernel of the stream until it completes.  Only the copy warp
+    // (before its first load) and the softmax warps (before their first store)
+    // touch global memory, and each waits for that completion there, so the
+    // roles' first-unit set-up overlaps the previous kernel's tail.  Dependents
+    // of this kernel may be scheduled from now on (they wait in the same way).
     griddep_launch_dependents();
     // Allocating all 512 columns can only start at lane 0, column 0, so the TMEM
     // base is the constant 0 (which keeps every TMEM address a compile-time
     // offset).  Anything else is reported and no work is done.
     constexpr uint32_t tmem = 0;
     const bool tmem_ok = misc[0] == 0u;
-    if (!tmem_ok && threadIdx.x == 0) atomicCAS(p.status, 0u, kStatusTmem);
+    if (!tmem_ok && threadIdx.x == 0) {
+        griddep_wait();
+        atomicCAS(p.status, 0u, kStatusTmem);
+    }
 
     // Waits in every role are polled by all 32 lanes and their outcome made
     // warp-uniform, so warp-collective instructions after them never diverge.
@@ -626,6 +640,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             uint32_t qused = 0;          // bit q: Q slot q has been loaded
             uint32_t nunit = 0;          // units of this CTA so far
             bool ok = p.inject != 1;
+            bool dep = false;            // the previous kernel has completed
+            auto dep_wait = [&]() {
+                if (!dep) {
+                    griddep_wait();
+                    dep = true;
+                }
+            };
             for (int r = 0; r < rounds && ok; ++r) {
                 const int u = unit_of(p, cta, G, r);
                 if (u >= p.n_units) continue;
@@ -639,6 +660,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     ok = wait_warp(bar(C::B_QEMPTY + q), ((qpar >> q) & 1u) ^ 1u, kSiteQEmpty);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::B_QFULL + q), C::TILE_BYTES);
+                    dep_wait();
                     const uint32_t dst = s_base + C::OFF_Q + q * C::TILE_BYTES;
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_3d(dst + c * C::CHUNK_BYTES, &tmap_q, c * 64, U.qt[w] * BM, U.bh,
@@ -655,6 +677,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         ok = wait_warp(bar(C::B_KVEMPTY + slot), ((rc / C::RING) & 1u) ^ 1u,
                                        kSiteKvEmpty);
                         if (!ok) break;
+                        dep_wait();
                         const uint32_t dst = s_base + C::OFF_RING + slot * C::ENTRY_BYTES;
                         if (FP8V && kind == 1) {
                             // V^T: one box of 128 keys (128 bytes) x V8_ROWS head-dim rows
@@ -682,10 +705,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     }
                 };
                 if constexpr (PAIR) {
-                    // per key tile: K, then V
+                    // per key tile: K, then V.  In the CTA's first unit the rest of
+                    // the ring waits until the first K has landed: every CTA starts
+                    // at once, and the first S should not queue behind the whole
+                    // grid's ring fill.
+                    bool first = nunit == 1;
                     for (int j = U.ulo; j < U.uhi && ok; ++j) {
                         if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
+                        const uint32_t kpos = rc;
                         load_kv(0, j);
+                        if (first && ok) {
+                            ok = wait_warp(bar(C::B_KVFULL + kpos % C::RING), (kpos / C::RING) & 1u, kSiteKvFullK);
+                            first = false;
+                        }
                         load_kv(1, j);
                     }
                 } else {
@@ -960,6 +992,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         Count2 sn, made, seen;        // per S buffer: S-ready waits, P tiles handed
                                       // to the MMA warp, P.V completions confirmed
         bool ok = true;
+        bool dep = false;             // the previous kernel has completed
 
         auto wait_pv = [&](int b) -> bool {
             if (seen.get(b) < made.get(b)) {
@@ -1298,24 +1331,63 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             tc_fence_after();
             const float inv_l = 1.f / l;
             const uint32_t o_addr = tmem + lane_off + C::o_col(PAIR ? wg : 0);
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
-                                                   ((static_cast<size_t>(U.bh) * p.L + i) * p.d_out) * 2);
+            if (!dep) {
+                griddep_wait();
+                dep = true;
+            }
+            if constexpr (C::OSTAGE) {
+                // The row's 16-byte chunks go to the warp's slab in the 128-byte
+                // swizzled layout of the O map's 64 x 32 box (chunk index XOR row
+                // mod 8: each store instruction covers all banks), then one lane
+                // stores the warp's 32 rows; rows past L and columns past d_out
+                // lie outside the map and are not written.
+                const uint32_t slab = s_base + C::OFF_OST + static_cast<uint32_t>(warp) * C::OST_WARP_BYTES;
+                if (lane == 0) bulk_wait_read0();     // the slab's previous store has read it
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(o_addr + 32 * c, raw);
+                    tmem_wait_ld();
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * inv_l,
+                                             __uint_as_float(raw[2 * e + 1]) * inv_l);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t chunk = static_cast<uint32_t>(4 * c + v4);
+                        st_shared_v4(slab + static_cast<uint32_t>(lane) * 128u + ((chunk ^ (lane & 7u)) << 4),
+                                     w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int row0 = qt * BM + wq * 32;
+                if (lane == 0 && row0 < p.L) {
+                    tma_store_3d(&tmap_o, slab, 0, row0, U.bh);
+                    bulk_commit();
+                }
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
+                                                       ((static_cast<size_t>(U.bh) * p.L + i) * p.d_out) * 2);
 #pragma unroll 1
-            for (int c = 0; c < D / 32 && 32 * c < p.d_out; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(o_addr + 32 * c, raw);
-                tmem_wait_ld();
-                uint32_t w16[16];
+                for (int c = 0; c < D / 32 && 32 * c < p.d_out; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(o_addr + 32 * c, raw);
+                    tmem_wait_ld();
+                    uint32_t w16[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * inv_l,
-                                         __uint_as_float(raw[2 * e + 1]) * inv_l);
-                if (row_valid) {
+                    for (int e = 0; e < 16; ++e)
+                        w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * inv_l,
+                                             __uint_as_float(raw[2 * e + 1]) * inv_l);
+                    if (row_valid) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        if (32 * c + 8 * v4 < p.d_out)
-                            dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
-                                                         w16[4 * v4 + 3]);
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            if (32 * c + 8 * v4 < p.d_out)
+                                dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
+                                                             w16[4 * v4 + 3]);
+                    }
                 }
             }
             if (row_valid && p.lse != nullptr) {
@@ -1324,6 +1396,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     (m_use + lg2_approx(l)) * 0.69314718055994530942f;
             }
             tc_fence_before();
+        }
+        // staged O: the last stores complete before the CTA's shared memory goes
+        if constexpr (C::OSTAGE) {
+            if (lane == 0) bulk_wait0();
+            __syncwarp();
         }
     }
 
