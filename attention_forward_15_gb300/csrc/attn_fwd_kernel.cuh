@@ -86,7 +86,8 @@ struct Cfg {
     static constexpr int EPT = D == 256 ? 2 : 1;                 // entries per tile
     static constexpr int ENTRY_BYTES = TILE_BYTES / EPT;
     static constexpr int ENTRY_CHUNKS = CHUNKS / EPT;
-    static constexpr int RING = D == 64 ? 8 : 5;
+    // (D = 128 pair mode: four entries, leaving room for the staged O rows)
+    static constexpr int RING = D == 64 ? 8 : (PAIR ? 4 : 5);
     // SEP: P has columns of its own (D = 64 leaves room), so the next S of a
     // lane can be computed while the softmax still works on the current one.
     // Then a second MMA warp issues the P.V products, so that neither issuer's
@@ -136,11 +137,11 @@ struct Cfg {
     static constexpr int NQB = D == 64 ? 2 : 1;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQB * NQ * TILE_BYTES;
-    // OSTAGE (D = 64 separate-P mode): each softmax warp writes its 32 rows of
-    // O through a shared slab of its own with one TMA store.  A thread storing
-    // its own 128-byte row from registers touches 32 lines per instruction.
-    static constexpr bool OSTAGE = SEP;
-    static constexpr int OST_WARP_BYTES = 32 * D * 2;
+    // OSTAGE (pair modes): each softmax warp writes its 32 rows of O through a
+    // shared slab of its own, 64 columns (128 bytes a row) per TMA store.  A
+    // thread storing its own row from registers touches 32 lines per instruction.
+    static constexpr bool OSTAGE = PAIR;
+    static constexpr int OST_WARP_BYTES = 32 * 64 * 2;
     static constexpr int OFF_OST = OFF_RING + RING * ENTRY_BYTES;
     static constexpr int OFF_BAR = OFF_OST + (OSTAGE ? 4 * NWG * OST_WARP_BYTES : 0);
     // barrier indices
@@ -159,7 +160,7 @@ struct Cfg {
     static_assert(PAIR ? (2 * 128 + 2 * D <= 512) : (D == 256), "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(PAIR ? EPT == 1 : true, "pair modes keep whole-tile ring entries");
-    static_assert(!OSTAGE || D == 64, "staged O rows are one 128-byte swizzle row");
+    static_assert(!OSTAGE || D <= 128, "staged O: pair modes only");
 };
 
 // ------------------------------------------------------------ work units
@@ -705,11 +706,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     }
                 };
                 if constexpr (PAIR) {
-                    // per key tile: K, then V.  In the CTA's first unit the rest of
-                    // the ring waits until the first K has landed: every CTA starts
-                    // at once, and the first S should not queue behind the whole
-                    // grid's ring fill.
-                    bool first = nunit == 1;
+                    // per key tile: K, then V.  In the CTA's first unit of a grid
+                    // with more units than CTAs, the rest of the ring waits until the
+                    // first K has landed: every CTA starts at once, and the first S
+                    // should not queue behind the whole grid's ring fill.
+                    bool first = nunit == 1 && p.n_units > G;
                     for (int j = U.ulo; j < U.uhi && ok; ++j) {
                         if (!lane_uses(U, 0, j) && !lane_uses(U, 1, j)) continue;
                         const uint32_t kpos = rc;
@@ -1336,37 +1337,40 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 dep = true;
             }
             if constexpr (C::OSTAGE) {
-                // The row's 16-byte chunks go to the warp's slab in the 128-byte
-                // swizzled layout of the O map's 64 x 32 box (chunk index XOR row
-                // mod 8: each store instruction covers all banks), then one lane
-                // stores the warp's 32 rows; rows past L and columns past d_out
-                // lie outside the map and are not written.
+                // Per 64 columns: the row's 16-byte chunks go to the warp's slab in
+                // the 128-byte swizzled layout of the O map's 64 x 32 box (chunk
+                // index XOR row mod 8: each store instruction covers all banks),
+                // then one lane stores the warp's 32 rows; rows past L and columns
+                // past d_out lie outside the map and are not written.
                 const uint32_t slab = s_base + C::OFF_OST + static_cast<uint32_t>(warp) * C::OST_WARP_BYTES;
-                if (lane == 0) bulk_wait_read0();     // the slab's previous store has read it
-                __syncwarp();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(o_addr + 32 * c, raw);
-                    tmem_wait_ld();
-                    uint32_t w16[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * inv_l,
-                                             __uint_as_float(raw[2 * e + 1]) * inv_l);
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        const uint32_t chunk = static_cast<uint32_t>(4 * c + v4);
-                        st_shared_v4(slab + static_cast<uint32_t>(lane) * 128u + ((chunk ^ (lane & 7u)) << 4),
-                                     w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
                 const int row0 = qt * BM + wq * 32;
-                if (lane == 0 && row0 < p.L) {
-                    tma_store_3d(&tmap_o, slab, 0, row0, U.bh);
-                    bulk_commit();
+#pragma unroll 1
+                for (int hc = 0; hc < D / 64; ++hc) {
+                    if (lane == 0) bulk_wait_read0();     // the slab's previous store has read it
+                    __syncwarp();
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(o_addr + 64 * hc + 32 * c, raw);
+                        tmem_wait_ld();
+                        uint32_t w16[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * inv_l,
+                                                 __uint_as_float(raw[2 * e + 1]) * inv_l);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const uint32_t chunk = static_cast<uint32_t>(4 * c + v4);
+                            st_shared_v4(slab + static_cast<uint32_t>(lane) * 128u + ((chunk ^ (lane & 7u)) << 4),
+                                         w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.L && 64 * hc < p.d_out) {
+                        tma_store_3d(&tmap_o, slab, 64 * hc, row0, U.bh);
+                        bulk_commit();
+                    }
                 }
             } else {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
