@@ -598,31 +598,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::ENTRY_BYTES, 16, 1024);
             const uint32_t d_tmem = tmem + C::s_col(sbuf);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
-                mma_ss(d_tmem, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+            for (int c = 0; c < C::CHUNKS; ++c) {   // four k-steps (32 bytes apart) per box
+                const uint64_t off = c * (C::CHUNK_BYTES >> 4);
+                mma_ss_x4(d_tmem, qd + off, kd + off, 2, 2, IDESC_S, c > 0 ? 1u : 0u);
             }
         };
         // O += P V: k-step kk covers keys [16kk, 16kk+16) = 16 rows of 128 bytes;
         // consecutive 64-column boxes of V are C::CHUNK_BYTES apart (LBO).
-        auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate) {
+        // (then a commit of the issuing lane's MMAs to `done`)
+        auto issue_pv = [&](int sbuf, int ocol_idx, uint32_t vslot, bool accumulate, uint32_t done) {
             const uint32_t d_tmem = tmem + C::o_col(ocol_idx);
             if constexpr (FP8V) {
                 // V^T rows of 128 keys (128 bytes, K-major); k-step kk covers keys
                 // [32kk, 32kk+32): 32 bytes into the swizzled row, 8 P columns
                 const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, 16, 1024);
-                const uint32_t a_tmem = tmem + C::pf8_col(sbuf);
-#pragma unroll
-                for (int kk = 0; kk < BN / 32; ++kk)
-                    mma_ts_f8(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 2), IDESC_PV8,
-                              (accumulate || kk > 0) ? 1u : 0u);
+                const uint32_t a = tmem + C::pf8_col(sbuf);
+                static_assert(BN / 32 == 4, "one batch of four 32-key steps");
+                mma_ts_f8_x4(d_tmem, a, a + 8, a + 16, a + 24, vd, 2, IDESC_PV8, accumulate ? 1u : 0u);
+                mma_commit(done);
             } else {
                 const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, C::CHUNK_BYTES, 1024);
-                const uint32_t a_tmem = tmem + C::p_col(sbuf);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), IDESC_PV,
-                           (accumulate || kk > 0) ? 1u : 0u);
+                static_assert(BN / 16 == 8, "one batch of eight 16-key steps");
+                mma_ts_x8_commit(d_tmem, tmem + C::p_col(sbuf), vd, 128, IDESC_PV, accumulate ? 1u : 0u, done);
             }
         };
 
@@ -810,9 +807,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                        kSiteKvFullV))
                             return false;
                         tc_fence_after();
-                        issue_pv(w, w, vslot, npv[w] > 0);
+                        issue_pv(w, w, vslot, npv[w] > 0, bar(C::B_ODONE + w));
                         ++npv[w];
-                        mma_commit(bar(C::B_ODONE + w));
                         const bool other_needs = pend_j[1 - w] == pend_j[w];
                         pend_j[w] = -1;
                         if (!other_needs) mma_commit(bar(C::B_KVEMPTY + vslot));
@@ -876,11 +872,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             tc_fence_after();
                             const uint64_t kd = sdesc_sw128(ring_smem + kslot * C::ENTRY_BYTES, 16, 1024);
 #pragma unroll
-                            for (int kl = 0; kl < KS_PER_ENTRY; ++kl) {
-                                const int kk = e * KS_PER_ENTRY + kl;
-                                const uint64_t qoff = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
-                                const uint64_t koff = (kl >> 2) * (C::CHUNK_BYTES >> 4) + (kl & 3) * 2;
-                                mma_ss(d_tmem, qd + qoff, kd + koff, IDESC_S, kk > 0 ? 1u : 0u);
+                            for (int j = 0; j < C::ENTRY_CHUNKS; ++j) {   // four k-steps per box
+                                const int cq = e * C::ENTRY_CHUNKS + j;      // box of Q
+                                mma_ss_x4(d_tmem, qd + cq * (C::CHUNK_BYTES >> 4), kd + j * (C::CHUNK_BYTES >> 4), 2,
+                                          2, IDESC_S, cq > 0 ? 1u : 0u);
                             }
                             // this K entry is free once its k-steps are done
                             mma_commit(bar(C::B_KVEMPTY + kslot));
@@ -910,19 +905,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                             if constexpr (FP8V) {
                                 constexpr uint32_t IDESC_PVE8 = idesc_e5m2_f32acc(BM, NV);
                                 const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES, 16, 1024);
-                                const uint32_t a_tmem = tmem + C::pf8_col(b);
-#pragma unroll
-                                for (int kk = 0; kk < BN / 32; ++kk)
-                                    mma_ts_f8(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 2),
-                                              IDESC_PVE8, (t > 0 || kk > 0) ? 1u : 0u);
+                                const uint32_t a = tmem + C::pf8_col(b);
+                                mma_ts_f8_x4(d_tmem, a, a + 8, a + 16, a + 24, vd, 2, IDESC_PVE8, t > 0 ? 1u : 0u);
                             } else {
                                 const uint64_t vd = sdesc_sw128(ring_smem + vslot * C::ENTRY_BYTES,
                                                                 C::CHUNK_BYTES, 1024);
                                 const uint32_t a_tmem = tmem + C::p_col(b);
 #pragma unroll
-                                for (int kk = 0; kk < BN / 16; ++kk)
-                                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128),
-                                           IDESC_PVE, (t > 0 || kk > 0) ? 1u : 0u);
+                                for (int h = 0; h < BN / 64; ++h) {   // four 16-key steps per batch
+                                    const uint32_t a = a_tmem + 32 * h;
+                                    mma_ts_x4(d_tmem, a, a + 8, a + 16, a + 24, vd + static_cast<uint64_t>(h * 512),
+                                              128, IDESC_PVE, (t > 0 || h > 0) ? 1u : 0u);
+                                }
                             }
                             // this V entry is free once its part of P.V is done
                             mma_commit(bar(C::B_KVEMPTY + vslot));
@@ -968,9 +962,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (!ok) break;
                         ++pn[w];
                         tc_fence_after();
-                        issue_pv(w, w, vslot, npv[w] > 0);
+                        issue_pv(w, w, vslot, npv[w] > 0, bar(C::B_ODONE + w));
                         ++npv[w];
-                        mma_commit(bar(C::B_ODONE + w));
                     }
                     if (!ok) break;
                     mma_commit(bar(C::B_KVEMPTY + vslot));

@@ -236,6 +236,96 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// Batches of four MMAs issued by one elected lane.  The issuing warp shares its
+// SM sub-partition with compute warps, so the instructions it spends per MMA
+// bound the MMA rate; one elect and the descriptor steps inside one block keep
+// them few.  A descriptor's start address is its low 14 bits (16-byte units),
+// so a step within one operand buffer is a 32-bit add to the low word.  The
+// first MMA of a batch accumulates if `accumulate` != 0, the others always do.
+
+// (warp) four SS MMAs: A_k, B_k = a_desc, b_desc advanced by k * a_step, k * b_step.
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t a_step,
+                                          uint32_t b_step, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b32 al, ah, bl, bh;\n\t.reg .b64 a1, b1, a2, b2, a3, b3;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+        "add.u32 al, al, %3;\n\tadd.u32 bl, bl, %4;\n\tmov.b64 a1, {al, ah};\n\tmov.b64 b1, {bl, bh};\n\t"
+        "add.u32 al, al, %3;\n\tadd.u32 bl, bl, %4;\n\tmov.b64 a2, {al, ah};\n\tmov.b64 b2, {bl, bh};\n\t"
+        "add.u32 al, al, %3;\n\tadd.u32 bl, bl, %4;\n\tmov.b64 a3, {al, ah};\n\tmov.b64 b3, {bl, bh};\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %5, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %5, q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(a_step), "r"(b_step), "r"(idesc), "r"(accumulate));
+}
+
+// (warp) four TS MMAs: A from TMEM at a0..a3, B_k = b_desc advanced by k * b_step.
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint64_t b_desc, uint32_t b_step, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b32 bl, bh;\n\t.reg .b64 b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %8, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "mov.b64 {bl, bh}, %5;\n\t"
+        "add.u32 bl, bl, %6;\n\tmov.b64 b1, {bl, bh};\n\t"
+        "add.u32 bl, bl, %6;\n\tmov.b64 b2, {bl, bh};\n\t"
+        "add.u32 bl, bl, %6;\n\tmov.b64 b3, {bl, bh};\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %7, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], b1, %7, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], b2, %7, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], b3, %7, q;\n\t}" ::"r"(d_tmem),
+        "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b_desc), "r"(b_step), "r"(idesc), "r"(accumulate));
+}
+
+// (warp) eight TS MMAs with A from consecutive 8-column steps of TMEM (a_tmem +
+// 8k) and B_k = b_desc advanced by k * b_step, then a commit of the issuing
+// lane's MMAs to `bar`, all from one elected lane.
+__device__ __forceinline__ void mma_ts_x8_commit(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t b_step,
+                                                 uint32_t idesc, uint32_t accumulate, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b32 bl, bh, a;\n\t.reg .b64 b;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "mov.b64 {bl, bh}, %2;\n\tmov.b32 a, %1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %2, %4, p;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "add.u32 a, a, 8;\n\tadd.u32 bl, bl, %3;\n\tmov.b64 b, {bl, bh};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, q;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(b_step), "r"(idesc), "r"(accumulate), "r"(bar));
+}
+
+// (warp) the same with 8-bit operands (kind::f8f6f4, K = 32 per MMA).
+__device__ __forceinline__ void mma_ts_f8_x4(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint64_t b_desc, uint32_t b_step, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b32 bl, bh;\n\t.reg .b64 b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %8, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "mov.b64 {bl, bh}, %5;\n\t"
+        "add.u32 bl, bl, %6;\n\tmov.b64 b1, {bl, bh};\n\t"
+        "add.u32 bl, bl, %6;\n\tmov.b64 b2, {bl, bh};\n\t"
+        "add.u32 bl, bl, %6;\n\tmov.b64 b3, {bl, bh};\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %5, %7, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%2], b1, %7, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], b2, %7, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], b3, %7, q;\n\t}" ::"r"(d_tmem),
+        "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b_desc), "r"(b_step), "r"(idesc), "r"(accumulate));
+}
+
 // (warp) arrive once on `bar` when every tcgen05 operation the issuing lane
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

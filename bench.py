@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only the backward (attn_bwd) on --workload and print one line "
                          "(for profiler runs)")
+    ap.add_argument("--fp8v-only", action="store_true",
+                    help="time only the FP8 P.V variant (attn_fwd_fp8v) on --workload and print one "
+                         "line (for profiler runs)")
     ap.add_argument("--threads", type=int, default=None,
                     help="host threads of the CPU oracle (--impl reference and the CPU baseline; "
                          "default: every core)")
@@ -449,6 +452,18 @@ def main():
             print(json.dumps({"metric": "attention bwd TFLOP/s (2.5 x forward flops)", "workload": w.name,
                               "value": round(fb * world / (msb * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                               "ms_per_step": round(msb, 5), "steps": args.steps, "warmup": args.warmup}),
+                  flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
+    if args.fp8v_only:
+        f8, _ = af.work(w.B, w.H, w.L, w.D, w.mask, w.block_size, w.dtype)
+        ms8, _ = time_workload(af, w, dev, args.steps, args.warmup, fp8v=True)
+        ms8 = reduce_max(ms8, dist, dev)
+        if rank == 0:
+            print(json.dumps({"metric": "attention fwd TFLOP/s, FP8 P.V variant", "workload": w.name,
+                              "value": round(f8 * world / (ms8 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                              "ms_per_step": round(ms8, 5), "steps": args.steps, "warmup": args.warmup}),
                   flush=True)
         if dist:
             dist.destroy_process_group()
