@@ -140,7 +140,8 @@ struct BwdCfg {
     static constexpr int OFF_BAR = OFF_VEC + NS * VEC_BYTES;
     static constexpr int B_FIX = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_SFULL = 1 + 2 * NS;   // SFULL, PFULL: one per half
     static constexpr int B_PFULL = B_SFULL + 2, B_DONE = B_PFULL + 2, B_DRAIN = B_DONE + 1;
-    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int B_FIXT = B_DRAIN + 1;             // FIX_TMEM: fixed pair copied to TMEM
+    static constexpr int NBAR = B_FIXT + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // [0]: TMEM base, [1]: abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int HALF_BYTES = 64 * 128;          // 64 rows of a 128-byte-wide box
@@ -148,9 +149,16 @@ struct BwdCfg {
     __device__ static constexpr uint32_t col_dp(int h) { return 128u * static_cast<uint32_t>(h) + 64u; }
     // ACC0 (dV, dK/dV only) and ACC1 (dK or dQ) after the S and dP buffers
     static constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = DQ ? 256 : 256 + DA;
+    // FIX_TMEM (D = 64, where the columns allow it): the fixed pair also sits in
+    // TMEM (16-bit pairs, row = lane), so S and dP take their A operand from
+    // there and read only the streamed half-tile from shared memory (a
+    // shared/shared N = 64 product is bound by shared-memory bandwidth).
+    static constexpr bool FIX_TMEM = D == 64;
+    static constexpr uint32_t COL_F0 = COL_ACC1 + DA, COL_F1 = COL_F0 + D / 2;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(D == 64 || D == 128 || D == 256, "backward head dim");
     static_assert(COL_ACC1 + DA <= TMEM_COLS, "tensor memory budget");
+    static_assert(!FIX_TMEM || COL_F1 + D / 2 <= TMEM_COLS, "tensor memory budget (fixed pair)");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -271,6 +279,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         }
         mbar_init(bar(C::B_DONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
+        mbar_init(bar(C::B_FIXT), 8);   // FIX_TMEM: one arrival per copying warp
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -352,14 +361,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         // X = A B^T over the head dim for 64 rows of B: both K-major, k-step kk
         // = head-dim columns [16kk, 16kk+16): box kk/4 (fixed A: CHUNK_BYTES apart,
         // ring B: RCHUNK_BYTES apart), 32-byte offset kk%4.
+        // (FIX_TMEM: A is the fixed tile's copy in TMEM at column a_tcol)
+        auto issue_fs = [&](uint32_t a_tcol, uint32_t b, uint32_t dcol) {
+            const uint32_t a = tmem + a_tcol;
+            mma_ts_x4(tmem + dcol, a, a + 8, a + 16, a + 24, sdesc_sw128(b, 16, 1024), 2, IDESC_SS, 0u);
+        };
         auto issue_ss = [&](uint32_t a, uint32_t b, uint32_t dcol) {
-            const uint64_t ad = sdesc_sw128(a, 16, 1024), bd = sdesc_sw128(b, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t aoff = (kk >> 2) * (C::CHUNK_BYTES >> 4) + (kk & 3) * 2;
-                const uint64_t boff = (kk >> 2) * (C::RCHUNK_BYTES >> 4) + (kk & 3) * 2;
-                mma_ss(tmem + dcol, ad + aoff, bd + boff, IDESC_SS, kk > 0 ? 1u : 0u);
-            }
+            for (int c = 0; c < C::CHUNKS; ++c)   // four k-steps (32 bytes apart) per 64-column box
+                mma_ss_x4(tmem + dcol, sdesc_sw128(a + c * C::CHUNK_BYTES, 16, 1024),
+                          sdesc_sw128(b + c * C::RCHUNK_BYTES, 16, 1024), 2, 2, IDESC_SS, c > 0 ? 1u : 0u);
         };
         // ACC += A(TMEM, 16-bit pairs) B over 64 rows of B, B MN-major: k-step kk
         // = rows [16kk, 16kk+16); its 64-column boxes are RCHUNK_BYTES apart (DSPLIT:
@@ -368,20 +379,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         auto issue_acc = [&](uint32_t acol, uint32_t b, uint32_t dcol, bool accumulate) {
             const uint64_t bd =
                 sdesc_sw128(b + static_cast<uint32_t>(dc * (C::DA / 64) * C::RCHUNK_BYTES), C::RCHUNK_BYTES, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 64 / 16; ++kk)
-                mma_ts(tmem + dcol, tmem + acol + (kk >> 1) * 32 + (kk & 1) * 8,
-                       bd + static_cast<uint64_t>(kk * 128), IDESC_ACC, (accumulate || kk > 0) ? 1u : 0u);
+            const uint32_t a = tmem + acol;
+            mma_ts_x4(tmem + dcol, a, a + 8, a + 32, a + 40, bd, 128, IDESC_ACC, accumulate ? 1u : 0u);
         };
         // S_h and dP_h of the tile in ring stage `stage`
         auto issue_half = [&](int stage, int h) {
             const uint32_t r0 = s_base + C::OFF_RING + stage * 2 * C::TILE_BYTES + h * C::HALF_BYTES;
-            issue_ss(f0, r0, C::col_s(h));
-            issue_ss(f1, r0 + C::TILE_BYTES, C::col_dp(h));
+            if constexpr (C::FIX_TMEM) {
+                issue_fs(C::COL_F0, r0, C::col_s(h));
+                issue_fs(C::COL_F1, r0 + C::TILE_BYTES, C::col_dp(h));
+            } else {
+                issue_ss(f0, r0, C::col_s(h));
+                issue_ss(f1, r0 + C::TILE_BYTES, C::col_dp(h));
+            }
             mma_commit(bar(C::B_SFULL + h));
         };
         bool ok = nn > 0;
         if (ok) ok = wait_warp(bar(C::B_FIX), 0, kSiteQFull);
+        if constexpr (C::FIX_TMEM) {
+            if (ok) ok = wait_warp(bar(C::B_FIXT), 0, kSiteQFull);
+        }
         if constexpr (C::HALF_RING) {
             // One ring entry per 64-row half: its S and dP, then (once the half's
             // compute warps have written P and dS) its two accumulations, which
@@ -461,6 +478,32 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         const uint32_t cs = tmem + lane_off + C::col_s(h) + 32 * g;    // this group's S columns
         const uint32_t cd = tmem + lane_off + C::col_dp(h) + 32 * g;   // and dP columns
         bool ok = true;
+        if constexpr (C::FIX_TMEM) {
+            // warps 0-3 copy F0, warps 4-7 F1: each thread its row, the eight
+            // 16-byte chunks (128-byte swizzle: chunk index XOR row mod 8) as 32
+            // words of 16-bit pairs, k-step kk at columns 8kk..8kk+7
+            if (warp < 8 && nn > 0) {
+                ok = wait_warp(bar(C::B_FIX), 0, kSiteQFull);
+                if (ok) {
+                    const int which = warp >> 2;
+                    const uint32_t src = s_base + C::OFF_FIX + which * C::TILE_BYTES + static_cast<uint32_t>(row) * 128u;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = ld_shared_v4(src + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(row) & 7u)) << 4));
+                        w[4 * c] = v.x;
+                        w[4 * c + 1] = v.y;
+                        w[4 * c + 2] = v.z;
+                        w[4 * c + 3] = v.w;
+                    }
+                    tmem_st32(tmem + lane_off + (which ? C::COL_F1 : C::COL_F0), w);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_FIXT));
+                }
+            }
+        }
         for (int t = 0; t < nn && ok; ++t) {
             // ring entry of this group's half: the tile's (whole-tile ring) or the
             // half's own (HALF_RING, whose vectors then start at the half's rows)
