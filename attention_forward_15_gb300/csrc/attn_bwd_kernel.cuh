@@ -65,6 +65,13 @@ struct BwdParams {
                              // consumer's bounded wait runs out (0 in normal use)
 };
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------------ prep
 
 // Di = sum_d dO[i,d] O[i,d] (fp32) for every row of every head, stored as -Di

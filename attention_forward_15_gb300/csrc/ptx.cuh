@@ -164,13 +164,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 // ------------------------------------------------------------------ tcgen05
 
 // (warp) 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both
