@@ -566,10 +566,15 @@ def shape_workload(spec: str):
     if len(f) not in (6, 7):
         raise SystemExit("--shape wants B,H,L,D,MASK,DTYPE[,BS]")
     masks = {v: k for k, v in MASK_NAMES.items()}
+    dtypes = {"fp16": torch.float16, "bf16": torch.bfloat16}
+    if f[4] not in masks or f[5] not in dtypes:
+        raise SystemExit(f"--shape: MASK one of {sorted(masks)}, DTYPE one of {sorted(dtypes)}")
     B, H, L, D = (int(x) for x in f[:4])
     mask = masks[f[4]]
-    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[f[5]]
+    dt = dtypes[f[5]]
     bs = int(f[6]) if len(f) == 7 else 0
+    if (mask == masks["block_diag"]) != (bs > 0) or (bs > 0 and L % bs):
+        raise SystemExit("--shape: a block size (dividing L) for block_diag, and only for it")
     return Workload(f"{f[4]}_b{B}h{H}l{L}d{D}_{f[5]}" + (f"_bs{bs}" if bs else ""), B, H, L, D, mask, dt,
                     1.0 / math.sqrt(D), bs)
 
