@@ -26,9 +26,14 @@ struct DeviceState {
     unsigned int *status = nullptr;   // device status word written by timed-out waits
     bool smem_attr[6][2] = {};        // per (kernel, dtype): dynamic smem attribute set
     bool bwd_attr[3][2][2] = {};      // backward: per (head dim, dtype, dK/dV | dQ)
+    // backward: a second stream for the dQ kernel, forked from and joined back
+    // into the caller's stream by two events (created on the first backward)
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 std::mutex g_mutex;
+std::mutex g_bwd_mutex;   // one backward's fork/launch/join sequence at a time
 DeviceState g_dev[kMaxDevices];
 int g_inject = 0;   // fault-injection mode for the next attn_fwd calls (tests only)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -593,15 +598,33 @@ template <int D, bool BF16>
 int bwd_for_dim(DeviceState &st, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                 const CUtensorMap &tg, const CUtensorMap &sq, const CUtensorMap &sk, const CUtensorMap &sv,
                 const CUtensorMap &sg, attn::BwdParams prm, void *dq, void *dk, void *dv, cudaStream_t s) {
+    // The dQ kernel needs only the prep kernel's vectors, not dK/dV: it runs on a
+    // second stream forked after the prep kernel and joined back before return,
+    // so its CTAs take the SMs the last wave of dK/dV leaves idle.  The fork/join
+    // is held under the library lock, so that concurrent callers cannot
+    // interleave the shared events, and is legal inside stream capture.
+    std::lock_guard<std::mutex> lk(g_bwd_mutex);
+    if (!st.side) {
+        if (cudaStreamCreateWithFlags(&st.side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&st.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&st.join, cudaEventDisableTiming) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    if (cudaEventRecord(st.fork, s) != cudaSuccess || cudaStreamWaitEvent(st.side, st.fork, 0) != cudaSuccess)
+        return ATTN_ERR_CUDA;
     // dK/dV: fixed K, V; streamed Q, dO
     prm.g0 = dk;
     prm.g1 = dv;
     int rc = launch_bwd<D, BF16, false>(st, tk, tv, sq, sg, prm, s);
-    if (rc != ATTN_OK) return rc;
     // dQ: fixed Q, dO; streamed K, V
     prm.g0 = dq;
     prm.g1 = nullptr;
-    return launch_bwd<D, BF16, true>(st, tq, tg, sk, sv, prm, s);
+    if (rc == ATTN_OK) rc = launch_bwd<D, BF16, true>(st, tq, tg, sk, sv, prm, st.side);
+    // the caller's stream waits for the dQ kernel (joined even after a failed
+    // launch, so that the side stream never stays forked)
+    if (cudaEventRecord(st.join, st.side) != cudaSuccess || cudaStreamWaitEvent(s, st.join, 0) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return rc;
 }
 
 }  // namespace
