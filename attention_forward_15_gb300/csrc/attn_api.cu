@@ -157,6 +157,24 @@ int encode_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype,
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 3-D tensor map over a [BH, L, D] 16-bit output for the backward's stores:
+// box = 32 columns (64 bytes) x 32 rows x 1 head, 64-byte swizzle; the part of
+// a box past L or D is not written.
+int encode_store_map(CUtensorMap *m, const void *ptr, int BH, int L, int D, int dtype) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // 3-D tensor map over V^T as float8 e5m2 bytes, [BH, D, L] with keys innermost:
 // box = 128 keys (128 bytes) x `rows` head-dim rows, 128-byte swizzle; rows
 // past D read as zero.
@@ -560,7 +578,8 @@ size_t bwd_workspace_bytes(long long BH, int L) {
 
 template <int D, bool BF16, bool DQ>
 int launch_bwd(DeviceState &st, const CUtensorMap &f0, const CUtensorMap &f1, const CUtensorMap &r0,
-               const CUtensorMap &r1, const attn::BwdParams &prm, cudaStream_t stream) {
+               const CUtensorMap &r1, const CUtensorMap &g0, const CUtensorMap &g1, const attn::BwdParams &prm,
+               cudaStream_t stream) {
     using C = attn::BwdCfg<D, DQ>;
     auto kern = attn::attn_bwd_kernel<D, BF16, DQ>;
     {
@@ -584,7 +603,7 @@ int launch_bwd(DeviceState &st, const CUtensorMap &f0, const CUtensorMap &f1, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, f0, f1, r0, r1, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, f0, f1, r0, r1, g0, g1, prm) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
@@ -612,14 +631,21 @@ int bwd_for_dim(DeviceState &st, const CUtensorMap &tq, const CUtensorMap &tk, c
     }
     if (cudaEventRecord(st.fork, s) != cudaSuccess || cudaStreamWaitEvent(st.side, st.fork, 0) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    // output maps (dK, dV, dQ) for the kernels' staged stores
+    const int dt = BF16 ? ATTN_BF16 : ATTN_F16;
+    CUtensorMap mdk, mdv, mdq, none;
+    std::memset(&none, 0, sizeof(none));
+    int rc = encode_store_map(&mdk, dk, prm.BH, prm.L, prm.d_out, dt);
+    if (rc == ATTN_OK) rc = encode_store_map(&mdv, dv, prm.BH, prm.L, prm.d_out, dt);
+    if (rc == ATTN_OK) rc = encode_store_map(&mdq, dq, prm.BH, prm.L, prm.d_out, dt);
     // dK/dV: fixed K, V; streamed Q, dO
     prm.g0 = dk;
     prm.g1 = dv;
-    int rc = launch_bwd<D, BF16, false>(st, tk, tv, sq, sg, prm, s);
+    if (rc == ATTN_OK) rc = launch_bwd<D, BF16, false>(st, tk, tv, sq, sg, mdk, mdv, prm, s);
     // dQ: fixed Q, dO; streamed K, V
     prm.g0 = dq;
     prm.g1 = nullptr;
-    if (rc == ATTN_OK) rc = launch_bwd<D, BF16, true>(st, tq, tg, sk, sv, prm, st.side);
+    if (rc == ATTN_OK) rc = launch_bwd<D, BF16, true>(st, tq, tg, sk, sv, mdq, none, prm, st.side);
     // the caller's stream waits for the dQ kernel (joined even after a failed
     // launch, so that the side stream never stays forked)
     if (cudaEventRecord(st.join, st.side) != cudaSuccess || cudaStreamWaitEvent(s, st.join, 0) != cudaSuccess)

@@ -245,6 +245,7 @@ template <int D, bool BF16, bool DQ>
 __global__ void __launch_bounds__(BwdCfg<D, DQ>::THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant__ CUtensorMap tm_f1,
                 const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
+                const __grid_constant__ CUtensorMap tm_g0, const __grid_constant__ CUtensorMap tm_g1,
                 const BwdParams p) {
     using C = BwdCfg<D, DQ>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -551,11 +552,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         if (ok && nn > 0) ok = wait_warp(bar(C::B_DONE), 0, kSiteODone);
         if (ok && nn > 0) {
             tc_fence_after();
-            const bool row_valid = row_idx < p.L;
             // 32-column jobs: ACC1 (dK or dQ, times sm_scale) to g0, and (dK/dV)
             // ACC0 (dV) to g1, dealt round-robin to the four groups; the
-            // accumulators hold head-dim columns [dc * DA, dc * DA + DA)
+            // accumulators hold head-dim columns [dc * DA, dc * DA + DA).  A job's
+            // 32 rows of the warp go through a 2 KB slab of the fixed-tile area
+            // (free once the last MMA is done) in the 64-byte swizzled layout of
+            // the output map's 32 x 32 box (16-byte chunk index XOR (row / 2) mod
+            // 4), then one lane stores them; rows past L and columns past d_out
+            // lie outside the map and are not written.
             constexpr int NJ = (DQ ? 1 : 2) * (C::DA / 32);
+            static_assert(16 * 2048 <= 2 * C::TILE_BYTES, "output slabs fit the fixed-tile area");
+            const uint32_t slab = s_base + C::OFF_FIX + static_cast<uint32_t>(warp) * 2048u;
+            const int row0 = f * 128 + (warp & 3) * 32;
 #pragma unroll 1
             for (int jb = wg; jb < NJ; jb += 4) {
                 const bool to_g0 = jb < C::DA / 32;
@@ -564,9 +572,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
                 if (col0 >= p.d_out) continue;
                 const uint32_t acol = to_g0 ? C::COL_ACC1 : C::COL_ACC0;
                 const float mul = to_g0 ? p.scale : 1.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(to_g0 ? p.g0 : p.g1) +
-                                                       ((static_cast<size_t>(bh) * p.L + row_idx) * p.d_out +
-                                                        static_cast<size_t>(dc) * C::DA) * 2);
                 uint32_t raw[32];
                 tmem_ld32(tmem + lane_off + acol + 32 * c, raw);
                 tmem_wait_ld();
@@ -574,15 +579,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     w16[e] = pack2<BF16>(__uint_as_float(raw[2 * e]) * mul, __uint_as_float(raw[2 * e + 1]) * mul);
-                if (row_valid) {
+                if (lane == 0) bulk_wait_read0();     // the slab's previous store has read it
+                __syncwarp();
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        if (col0 + 8 * v4 < p.d_out)
-                            dst[c * 4 + v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2],
-                                                         w16[4 * v4 + 3]);
+                for (int v4 = 0; v4 < 4; ++v4)
+                    st_shared_v4(slab + static_cast<uint32_t>(lane) * 64u +
+                                     ((static_cast<uint32_t>(v4) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4),
+                                 w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 < p.L) {
+                    tma_store_3d(to_g0 ? &tm_g0 : &tm_g1, slab, col0, row0, bh);
+                    bulk_commit();
                 }
             }
         }
+        // the output stores complete before the CTA's shared memory goes
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
         tc_fence_before();
     }
 
