@@ -32,9 +32,9 @@
 // buffers of its own in tensor memory, so the MMA pipe computes one half's
 // products while the compute warps work on the other:
 //   S_0 | dP_0 | S_1 | dP_1 (64 columns each) | ACC0 (D) | ACC1 (D).
-// Each half is split between two warpgroups of 32 columns; a group writes its
-// P (16-bit pairs) over the first 16 of its S columns and its dS over the
-// first 16 of its dP columns, once read; a half's next S and dP
+// All four compute warpgroups take each half in turn, 16 columns a group; a
+// group writes its P (16-bit pairs) over the first 8 of its S columns and its
+// dS over the first 8 of its dP columns, once read; a half's next S and dP
 // are issued after the products that read its P and dS, on the same in-order
 // MMA pipe.  D is 64 or 128 (256 + 2D columns), or 256: then the fixed pair
 // fills 128 KB of shared memory, the ring holds one 64-row half of the streamed
@@ -135,7 +135,7 @@ struct BwdCfg {
     // dV (two CTAs per key tile, both computing S and dP over the whole head dim)
     static constexpr bool DSPLIT = HALF_RING && !DQ;
     static constexpr int DA = DSPLIT ? D / 2 : D;        // accumulator width (columns)
-    // four compute warpgroups (group w takes 32 of the 64 rows of half w/2 of
+    // four compute warpgroups (group w takes 16 of the 64 rows of each half of
     // every streamed tile), a TMA warp and an MMA warp
     static constexpr int THREADS = 576;
     static constexpr int WARP_TMA = 16, WARP_MMA = 17;
@@ -283,7 +283,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar(C::B_SFULL + h), 1);
-            mbar_init(bar(C::B_PFULL + h), 8);   // one arrival per warp of half h's two groups
+            mbar_init(bar(C::B_PFULL + h), 16);   // one arrival per compute warp
         }
         mbar_init(bar(C::B_DONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
@@ -382,13 +382,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         };
         // ACC += A(TMEM, 16-bit pairs) B over 64 rows of B, B MN-major: k-step kk
         // = rows [16kk, 16kk+16); its 64-column boxes are RCHUNK_BYTES apart (DSPLIT:
-        // starting at the head-dim half dc).  The A pairs of rows [32g, 32g+32)
-        // sit at columns 32g..32g+15 of the half.
+        // starting at the head-dim half dc).  The A pairs of rows [16kk, 16kk+16)
+        // sit at columns 16kk..16kk+7 of the half.
         auto issue_acc = [&](uint32_t acol, uint32_t b, uint32_t dcol, bool accumulate) {
             const uint64_t bd =
                 sdesc_sw128(b + static_cast<uint32_t>(dc * (C::DA / 64) * C::RCHUNK_BYTES), C::RCHUNK_BYTES, 1024);
             const uint32_t a = tmem + acol;
-            mma_ts_x4(tmem + dcol, a, a + 8, a + 32, a + 40, bd, 128, IDESC_ACC, accumulate ? 1u : 0u);
+            mma_ts_x4(tmem + dcol, a, a + 16, a + 32, a + 48, bd, 128, IDESC_ACC, accumulate ? 1u : 0u);
         };
         // S_h and dP_h of the tile in ring stage `stage`
         auto issue_half = [&](int stage, int h) {
@@ -469,11 +469,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
         __syncwarp();
     } else {
         // ================================================================ compute warps
-        // group wg takes columns [32g, 32g+32) of half h = wg/2 (g = wg%2) of every
-        // streamed tile; each thread owns one TMEM lane, i.e. one row of the
-        // fixed tile
+        // group wg takes columns [16wg, 16wg+16) of each half of every streamed
+        // tile, half 0 then half 1; each thread owns one TMEM lane, i.e. one row
+        // of the fixed tile
         const int wg = warp >> 2;
-        const int h = wg >> 1, g = wg & 1;
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int row_idx = f * 128 + row;                 // query (dQ) or key (dK/dV) index
@@ -483,8 +482,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             row_nl = p.nlse2[static_cast<size_t>(bh) * p.n_pad + row_idx];
             row_nd = p.ndelta[static_cast<size_t>(bh) * p.n_pad + row_idx];
         }
-        const uint32_t cs = tmem + lane_off + C::col_s(h) + 32 * g;    // this group's S columns
-        const uint32_t cd = tmem + lane_off + C::col_dp(h) + 32 * g;   // and dP columns
         bool ok = true;
         if constexpr (C::FIX_TMEM) {
             // warps 0-3 copy F0, warps 4-7 F1: each thread its row, the eight
@@ -513,41 +510,43 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_f0, const __grid_constant
             }
         }
         for (int t = 0; t < nn && ok; ++t) {
-            // ring entry of this group's half: the tile's (whole-tile ring) or the
-            // half's own (HALF_RING, whose vectors then start at the half's rows)
-            const int s = C::HALF_RING ? (2 * t + h) % C::NS : t % C::NS;
             const int j = lo + t;
-            const float *vec = reinterpret_cast<const float *>(smem + C::OFF_VEC + s * C::VEC_BYTES);
             // tiles that cross the mask, and (dQ) a ragged last key tile
             const bool masked = (p.mask == kMaskCausal && j == f) || (p.mask == kMaskBlock && (p.bs % 128) != 0) ||
                                 (DQ && (j + 1) * 128 > p.L);
-            ok = wait_warp(bar(C::B_SFULL + h), t & 1, kSiteSFull);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+            for (int h = 0; h < 2 && ok; ++h) {
+                // ring entry of this half: the tile's (whole-tile ring) or the
+                // half's own (HALF_RING, whose vectors then start at the half's rows)
+                const int s = C::HALF_RING ? (2 * t + h) % C::NS : t % C::NS;
+                const float *vec = reinterpret_cast<const float *>(smem + C::OFF_VEC + s * C::VEC_BYTES);
+                const uint32_t cs = tmem + lane_off + C::col_s(h) + 16 * wg;    // this group's S columns
+                const uint32_t cd = tmem + lane_off + C::col_dp(h) + 16 * wg;   // and dP columns
+                ok = wait_warp(bar(C::B_SFULL + h), t & 1, kSiteSFull);
+                if (!ok) break;
+                tc_fence_after();
                 uint32_t sv[16], dpv[16];
-                tmem_ld16(cs + 16 * c, sv);
-                tmem_ld16(cd + 16 * c, dpv);
+                tmem_ld16(cs, sv);
+                tmem_ld16(cd, dpv);
                 tmem_wait_ld();
                 uint32_t pk[8], dk[8];
-                const int c0 = 64 * h + 32 * g + 16 * c;     // column of the sub-chunk in the tile
-                const int vc0 = C::HALF_RING ? c0 - 64 * h : c0;
+                const int c0 = 64 * h + 16 * wg;              // column of the chunk in the tile
+                const int vc0 = C::HALF_RING ? 16 * wg : c0;
                 if (masked)
                     bwd_chunk<BF16, DQ, true, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + C::VEC_ROWS, c0, vc0,
                                                   p.mask, p.bs, p.L, row_idx, j * 128, pk, dk);
                 else
                     bwd_chunk<BF16, DQ, false, 16>(sv, dpv, sc, row_nl, row_nd, vec, vec + C::VEC_ROWS, c0, vc0,
                                                    p.mask, p.bs, p.L, row_idx, j * 128, pk, dk);
-                // P and dS of sub-chunk c to columns [8c, 8c+8) of this group's
-                // S and dP columns, which it has read by now
-                if constexpr (!DQ) tmem_st8(cs + 8 * c, pk);
-                tmem_st8(cd + 8 * c, dk);
+                // P and dS to the first 8 of this group's S and dP columns, which
+                // it has read by now
+                if constexpr (!DQ) tmem_st8(cs, pk);
+                tmem_st8(cd, dk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_PFULL + h));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_PFULL + h));
         }
         if (ok && nn > 0) ok = wait_warp(bar(C::B_DONE), 0, kSiteODone);
         if (ok && nn > 0) {
