@@ -282,7 +282,9 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     """``attn_bwd``: gradients ``(dq, dk, dv)`` of ``sum(dout * o)`` for the
     forward ``fwd(q, k, v, mask_kind, block_size, sm_scale)`` that returned
     ``(o, lse)``.  All CUDA tensors, contiguous, q/k/v/o/dout [B, H, L, D]
-    fp16/bf16 (D <= 128), lse float32 [B, H, L].  Asynchronous on ``stream``."""
+    fp16/bf16 (D a multiple of 8 up to 256), lse float32 [B, H, L].
+    Asynchronous on ``stream`` (the dQ kernel runs on a second stream of the
+    library, forked from and joined back into ``stream``)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         if not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA [B, H, L, D] tensor")

@@ -118,6 +118,39 @@ def test_bwd_deterministic(af):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_bwd_in_cuda_graph(af, D):
+    """The backward captured in a CUDA graph (its dQ kernel runs on a stream
+    forked from the capturing one and joined back) replays to the eager
+    result, bit for bit, twice."""
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in make_qkv(2, 4, 384, D, torch.float16, seed=11))
+    g = _dout(q.cpu(), 12).to(dev)
+    o, lse = af.fwd(q, k, v, CAUSAL)
+    ref = af.bwd(q, k, v, o, lse, g, CAUSAL)
+    outs = tuple(torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(max(16, af.load_library().attn_bwd_workspace_size(2, 4, 384)), dtype=torch.uint8,
+                     device=dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):      # warm-up outside the capture
+        af.bwd(q, k, v, o, lse, g, CAUSAL, dq=outs[0], dk=outs[1], dv=outs[2], workspace=ws)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        af.bwd(q, k, v, o, lse, g, CAUSAL, dq=outs[0], dk=outs[1], dv=outs[2], workspace=ws)
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        for x, y in zip(outs, ref):
+            assert torch.equal(x, y)
+    st, _ = af.last_device_status(0)
+    assert st == 0
+
+
 def test_bwd_argument_errors(af):
     dev = torch.device("cuda", 0)
     q = torch.zeros((1, 1, 128, 100), dtype=torch.float16, device=dev)
