@@ -260,7 +260,13 @@ int attn_debug_inject(int mode);
  *                     other arguments as for attn_fwd.
  * Every pointer must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
  *
- * Three kernels run in order on `stream`.  Returns ATTN_OK once enqueued;
+ * Three kernels: the row-statistics kernel and the dK/dV kernel on `stream`,
+ * the dQ kernel (which needs only the former) on a second stream the library
+ * owns, forked from `stream` after the row-statistics kernel and joined back
+ * into it before the call returns, so work enqueued on `stream` afterwards
+ * waits for all three.  The fork and join use events and are valid inside
+ * stream capture; concurrent calls serialise only their enqueueing.
+ * Returns ATTN_OK once enqueued;
  * ATTN_ERR_ARG if workspace_bytes is too small or sm_scale is not finite;
  * argument errors as attn_fwd, all before any CUDA call; device-side
  * timeouts are reported through attn_last_device_status.
