@@ -55,6 +55,7 @@ _SIGNATURES = {
     "attn_fwd_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
                          [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "attn_bwd_work": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_double)] * 2),
+    "attn_fwd_host_chunks": (ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_int)] * 2),
 }
 
 _lib = None
@@ -120,6 +121,18 @@ def plan(B: int, H: int, L: int, D: int, mask_kind: int, block_size: int = 0,
     if with_ctas:
         out["ctas"] = c.value
     return out
+
+
+def host_chunks(B: int, H: int, L: int, D: int, mask_kind: int, block_size: int = 0,
+                dtype: torch.dtype = torch.float16, sms: int = 152) -> tuple[int, int]:
+    """(heads per chunk, chunks) that ``fwd_host`` pipelines on a device with
+    ``sms`` SMs (host arithmetic only)."""
+    hc, n = ctypes.c_int(), ctypes.c_int()
+    rc = load_library().attn_fwd_host_chunks(B, H, L, D, mask_kind, block_size, _dtype_code(dtype), sms,
+                                             ctypes.byref(hc), ctypes.byref(n))
+    if rc:
+        raise AttnError(rc, "attn_fwd_host_chunks")
+    return hc.value, n.value
 
 
 def last_device_status(device: int = 0) -> tuple[int, int]:
@@ -213,7 +226,8 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int =
              staging: dict | None = None, return_lse: bool = True):
     """Forward of HOST tensors through ``attn_fwd_host``: the library copies q,
     k, v to the GPU, runs the forward on the current stream of ``device``,
-    copies o and lse back and synchronises.  ``staging`` keeps the device
+    copies o and lse back and synchronises, pipelined over chunks of heads
+    (``host_chunks``) so that both copy directions and the kernels overlap.  ``staging`` keeps the device
     buffers (``q_d, k_d, v_d, o_d, lse_d``) and the page-locked host outputs
     (``o_h, lse_h``) for reuse across calls.  Returns ``(o_host, lse_host)``."""
     lib = load_library()

@@ -15,8 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libattn_gb300.so"
-SOURCES = ["attn_api.cu"]
-DEPENDS = ["attn_api.cu", "attn_fwd_kernel.cuh", "attn_bwd_kernel.cuh", "ptx.cuh"]
+SOURCES = ["attn_api.cu", "attn_host.cu"]
+DEPENDS = ["attn_api.cu", "attn_host.cu", "attn_fwd_kernel.cuh", "attn_bwd_kernel.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -405,34 +405,6 @@ int attn_fwd_fp8v(const void *q, const void *k, const void *vt, void *o, float *
     return fwd_common<true>(q, k, vt, o, lse, B, H, L, D, mask_kind, block_size, sm_scale, dtype, stream);
 }
 
-int attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
-                  void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d, int B, int H, int L,
-                  int D, int mask_kind, int block_size, float sm_scale, int dtype, void *stream) {
-    int rc = validate_shape(B, H, L, D, mask_kind, block_size, dtype);
-    if (rc != ATTN_OK) return rc;
-    if (!std::isfinite(sm_scale)) return ATTN_ERR_ARG;
-    if (static_cast<long long>(B) * H * L == 0) return ATTN_OK;   // empty problem
-    if (!q_h || !k_h || !v_h || !o_h || !q_d || !k_d || !v_d || !o_d || (lse_h && !lse_d))
-        return ATTN_ERR_NULL;
-    if (!aligned16(q_d) || !aligned16(k_d) || !aligned16(v_d) || !aligned16(o_d) ||
-        (lse_d && !aligned16(lse_d)))
-        return ATTN_ERR_ALIGN;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes = static_cast<size_t>(B) * H * L * D * 2;
-    const size_t lse_bytes = static_cast<size_t>(B) * H * L * sizeof(float);
-    if (cudaMemcpyAsync(q_d, q_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(k_d, k_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(v_d, v_h, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return ATTN_ERR_CUDA;
-    rc = attn_fwd(q_d, k_d, v_d, o_d, lse_h ? lse_d : nullptr, B, H, L, D, mask_kind, block_size,
-                  sm_scale, dtype, stream);
-    if (rc != ATTN_OK) return rc;
-    if (cudaMemcpyAsync(o_h, o_d, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (lse_h && cudaMemcpyAsync(lse_h, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return ATTN_ERR_CUDA;
-    return cudaStreamSynchronize(s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
 int attn_last_device_status(int device, int *status, unsigned int *detail) {
     if (!status) return ATTN_ERR_NULL;
     if (device < 0 || device >= kMaxDevices) return ATTN_ERR_ARG;

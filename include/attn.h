@@ -209,16 +209,33 @@ int attn_fwd_fp8v_check(const void *q, const void *k, const void *vt, const void
  *                   may reuse across calls (lse_d may be NULL when lse_h is).
  *   the rest        as for attn_fwd.
  *
- * One cudaMemcpyAsync per tensor, then the kernel, on `stream`.  Returns an
- * attn_status: argument errors as attn_fwd (plus ATTN_ERR_NULL for a missing
- * host or device buffer) before any copy; ATTN_ERR_CUDA if a copy, the launch
- * or the synchronisation fails.  A device-side timeout is read with
- * attn_last_device_status, as for attn_fwd.
+ * The B*H heads are cut into chunks (attn_fwd_host_chunks) that flow through
+ * three stages at once: the library's copy-in stream copies chunk c+1's q, k, v
+ * while `stream` runs the forward of chunk c and the library's copy-out stream
+ * copies chunk c-1's o and lse back.  Both copy streams start after the work
+ * already queued on `stream`, and `stream` waits for both before the call
+ * synchronises it.  Each chunk's forward is attn_fwd over that chunk's heads;
+ * the results are those of one attn_fwd over all of them (no mask depends on
+ * the head).  Calls from several host threads are serialised while they
+ * enqueue.  Returns an attn_status: argument errors as attn_fwd (plus
+ * ATTN_ERR_NULL for a missing host or device buffer) before any copy;
+ * ATTN_ERR_CUDA if a copy, a launch or the synchronisation fails (the copies
+ * already queued still finish before the call returns).  A device-side timeout
+ * is read with attn_last_device_status, as for attn_fwd.
  */
 int attn_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
                   void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
                   int B, int H, int L, int D, int mask_kind, int block_size,
                   float sm_scale, int dtype, void *stream);
+
+/* The chunking attn_fwd_host uses on a device with `sms` SMs: heads per
+ * chunk and number of chunks (both 0 for an empty problem).  Pure host
+ * arithmetic, no CUDA call: the count minimises a three-stage pipeline model
+ * (copy in, forward, copy out) with rates measured on GB300, at most 16
+ * chunks.  Returns ATTN_ERR_ARG for sms <= 0, else as attn_fwd_check's shape
+ * checks. */
+int attn_fwd_host_chunks(int B, int H, int L, int D, int mask_kind, int block_size, int dtype, int sms,
+                         int *heads_per_chunk, int *chunks);
 
 /* Number of work units and CTAs attn_fwd would launch for these arguments on
  * the current device (for tests and reports); returns an attn_status. */

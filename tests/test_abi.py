@@ -166,3 +166,27 @@ def test_bwd_host_side(lib):
     assert b(mask=2, bs=48) == 3
     assert b(L=0, ptr=0, wsp=0) == 0          # empty: nothing to do
     assert b() == 0
+
+
+def test_host_chunking(lib):
+    """attn_fwd_host's chunk choice: the chunks cover every head once, stay
+    within 16, keep each chunk's lse slice 16-byte aligned, are one chunk for a
+    problem too small to pipeline, and several for the copy-bound headline."""
+    import attention_forward_15_gb300 as af
+    for B, H, L, D, mask, bs in [(4, 16, 1024, 64, 0, 0), (2, 32, 4096, 128, 1, 0), (1, 2, 256, 128, 2, 64),
+                                 (8, 16, 8192, 128, 2, 64), (1, 32, 32768, 128, 1, 0),
+                                 (1, 16, 16384, 256, 0, 0), (5, 5, 2047, 64, 0, 0), (3, 7, 1001, 64, 1, 0),
+                                 (1, 1, 4096, 64, 0, 0), (2, 9, 333, 128, 0, 0), (64, 64, 128, 32, 1, 0)]:
+        for sms in (1, 152):
+            hc, n = af.host_chunks(B, H, L, D, mask, bs, sms=sms)
+            BH = B * H
+            assert 1 <= n <= 16 and 1 <= hc <= BH, (B, H, L, D, sms)
+            assert (n - 1) * hc < BH <= n * hc
+            if n > 1:
+                assert (hc * L * 4) % 16 == 0
+    assert af.host_chunks(1, 2, 256, 128, 2, 64) == (2, 1)
+    assert af.host_chunks(4, 16, 1024, 64, 0)[1] > 1
+    assert af.host_chunks(0, 16, 1024, 64, 0) == (0, 0)
+    hc, n = ctypes.c_int(), ctypes.c_int()
+    assert lib.attn_fwd_host_chunks(1, 1, 256, 64, 0, 0, 0, 0, ctypes.byref(hc), ctypes.byref(n)) == 8
+    assert lib.attn_fwd_host_chunks(1, 1, 256, 100, 0, 0, 0, 152, ctypes.byref(hc), ctypes.byref(n)) == 4

@@ -244,12 +244,17 @@ def test_host_buffer_entry_point(af, mask, bs, dt):
 
 
 @pytest.mark.parametrize("B,H,L,D,mask,dt", [(4, 16, 1024, 64, DENSE, torch.float16),
-                                             (3, 5, 1000, 128, CAUSAL, torch.bfloat16)])
+                                             (3, 11, 1000, 128, CAUSAL, torch.bfloat16),
+                                             (5, 5, 2047, 64, DENSE, torch.float16)])
 def test_host_entry_point_large(af, B, H, L, D, mask, dt):
-    """attn_fwd_host on the headline size and on a ragged causal D = 128 case:
-    the same bytes as attn_fwd on device buffers."""
-    q, k, v = (t.pin_memory() for t in make_qkv(B, H, L, D, dt, seed=8))
+    """attn_fwd_host on the headline size, on a ragged causal D = 128 case and
+    on L = 2047 (lse slices aligned by whole groups of heads, a shorter last
+    chunk): each is pipelined over several chunks and gives the same bytes as
+    one attn_fwd on device buffers."""
     dev = torch.device("cuda", 0)
+    hc, n = af.host_chunks(B, H, L, D, mask, 0, dt, torch.cuda.get_device_properties(dev).multi_processor_count)
+    assert n > 1 and hc * n >= B * H
+    q, k, v = (t.pin_memory() for t in make_qkv(B, H, L, D, dt, seed=8))
     o_ref, lse_ref = af.fwd(q.to(dev), k.to(dev), v.to(dev), mask, 0, 0.1)
     torch.cuda.synchronize()
     staging = {}
