@@ -190,3 +190,31 @@ def test_host_chunking(lib):
     hc, n = ctypes.c_int(), ctypes.c_int()
     assert lib.attn_fwd_host_chunks(1, 1, 256, 64, 0, 0, 0, 0, ctypes.byref(hc), ctypes.byref(n)) == 8
     assert lib.attn_fwd_host_chunks(1, 1, 256, 100, 0, 0, 0, 152, ctypes.byref(hc), ctypes.byref(n)) == 4
+
+
+def test_host_entry_point_rejections(lib):
+    """attn_fwd_host rejects before any copy or launch: attn_fwd's argument
+    checks on the device buffers, then a missing host buffer.  An empty
+    problem returns at once.  The placeholder addresses reach the launching
+    call only where no CUDA device exists, as for attn_fwd above."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("placeholder addresses go only to the check entry points when a GPU is present")
+    P = ctypes.c_void_p
+
+    def host(h=(16, 16, 16, 16), d=(16, 16, 16, 16), lse_h=None, lse_d=None, B=1, H=2, L=256, D=64, mask=0,
+             bs=0, scale=0.1, dtype=0):
+        hq, hk, hv, ho = (P(x) if x else None for x in h)
+        dq, dk, dv, do = (P(x) if x else None for x in d)
+        return lib.attn_fwd_host(hq, hk, hv, ho, lse_h, dq, dk, dv, do, lse_d, B, H, L, D, mask, bs, scale,
+                                 dtype, None)
+    assert host(D=100) == 4
+    assert host(mask=2, bs=48) == 3
+    assert host(scale=float("nan")) == 8
+    assert host(d=(16, 0, 16, 16)) == 1
+    assert host(d=(16, 16, 24, 16)) == 5
+    assert host(h=(16, 16, 16, 0)) == 1
+    assert host(h=(0, 16, 16, 16)) == 1
+    assert host(lse_h=P(32), lse_d=None) == 1
+    assert host(lse_h=P(32), lse_d=P(20)) == 5
+    assert host(B=0, h=(0, 0, 0, 0), d=(0, 0, 0, 0)) == 0

@@ -263,6 +263,46 @@ def test_host_entry_point_large(af, B, H, L, D, mask, dt):
         assert torch.equal(o_h, o_ref.cpu()) and torch.equal(lse_h, lse_ref.cpu())
 
 
+def test_host_entry_point_stream_order(af):
+    """attn_fwd_host on a non-default stream with work already queued on it:
+    the library's copy streams start after that work (here a long fill of the
+    device input buffers with NaN), so the uploads land after it and the
+    result equals attn_fwd's; and with lse not requested the chunked path
+    leaves the lse buffer untouched."""
+    import ctypes
+    lib = af.load_library()
+    dev = torch.device("cuda", 0)
+    B, H, L, D = 4, 16, 1024, 64
+    q, k, v = (t.pin_memory() for t in make_qkv(B, H, L, D, torch.float16, seed=11))
+    o_ref, lse_ref = af.fwd(q.to(dev), k.to(dev), v.to(dev), DENSE, 0, 0.125)
+    torch.cuda.synchronize()
+    qd, kd, vd, od = (torch.empty_like(q, device=dev) for _ in range(4))
+    lsed = torch.full((B, H, L), 7.0, dtype=torch.float32, device=dev)
+    oh = torch.empty_like(q).pin_memory()
+    lseh = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream(dev)
+    big = torch.empty(1 << 28, dtype=torch.float16, device=dev)   # 512 MB: a fill of a few tens of us
+
+    def call(lse_h, lse_d):
+        return lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), oh.data_ptr(), lse_h,
+                                 qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), lse_d,
+                                 B, H, L, D, DENSE, 0, 0.125, 0, ctypes.c_void_p(s.cuda_stream))
+
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            big.fill_(1.0)
+            for t in (qd, kd, vd, od):
+                t.fill_(float("nan"))
+        assert call(lseh.data_ptr(), lsed.data_ptr()) == 0
+        assert torch.equal(oh, o_ref.cpu()) and torch.equal(lseh, lse_ref.cpu())
+    lsed.fill_(7.0)
+    torch.cuda.synchronize()
+    oh.zero_()
+    assert call(None, None) == 0
+    assert torch.equal(oh, o_ref.cpu())
+    assert bool((lsed == 7.0).all())
+
+
 def test_argument_errors(af):
     dev = torch.device("cuda", 0)
     q = torch.zeros((1, 1, 256, 100), dtype=torch.float16, device=dev)
