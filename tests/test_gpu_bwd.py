@@ -64,8 +64,9 @@ def _case(af, B, H, L, D, mask, bs, dt, scale=None, seed=42, qkv=None):
         worst = np.unravel_index(np.argmax(err - tol), err.shape)
         # the widest tolerance relative to the value, so a vacuous bound is visible
         big = np.abs(want) > 1e-3 * np.abs(want).max()
+        rel = (tol[big] / np.abs(want[big])).max() if big.any() else float("nan")   # nan: want is all zero
         print(f"bwd {name} B{B} H{H} L{L} D{D} mask{mask}: max err {err.max():.3e}, max tol {tol.max():.3e}, "
-              f"max tol/|ref| {(tol[big] / np.abs(want[big])).max():.3e}, max err/tol {(err / tol).max():.3f}")
+              f"max tol/|ref| {rel:.3e}, max err/tol {(err / tol).max():.3f}")
         assert (err <= tol).all(), (f"{name}: max(err - tol) = {(err - tol).max():.3e} at {worst} "
                                     f"(err {err[worst]:.3e}, tol {tol[worst]:.3e}, ref {want[worst]:.3e})")
 
@@ -96,6 +97,34 @@ CASES = [
     *c[:6], "f16" if c[6] == torch.float16 else "bf16"))
 def test_bwd_all_elements(af, case):
     _case(af, *case)
+
+
+# Seeded random configurations (drawn once, the same on every run): any head
+# dim, L from 1 to 600, each mask with its block sizes, both dtypes, a random
+# scale; combinations the chosen cases above do not name.
+def _random_cases(seed=20261204, n=12):
+    import random
+    rnd = random.Random(seed)
+    cases = []
+    for _ in range(n):
+        mask = rnd.choice([DENSE, CAUSAL, BLOCK_DIAG])
+        D = 8 * rnd.randint(1, 32)
+        if mask == BLOCK_DIAG:
+            bs = rnd.choice([1, 4, 16, 32, 64, 128, 256, 384])
+            L = bs * rnd.randint(1, max(1, 600 // bs))
+        else:
+            bs, L = 0, rnd.randint(1, 600)
+        dt = rnd.choice([torch.float16, torch.bfloat16])
+        cases.append((1, rnd.randint(1, 2), L, D, mask, bs, dt, round(rnd.uniform(0.02, 0.3), 4),
+                      rnd.randint(0, 10 ** 6)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "B{}H{}L{}D{}m{}bs{}{}s{}".format(
+    *c[:6], "f16" if c[6] == torch.float16 else "bf16", c[7]))
+def test_bwd_random_configurations(af, case):
+    B, H, L, D, mask, bs, dt, scale, seed = case
+    _case(af, B, H, L, D, mask, bs, dt, scale=scale, seed=seed)
 
 
 @pytest.mark.parametrize("sign", [1, -1])
