@@ -79,6 +79,34 @@ def test_fp8v_all_elements(af, case):
     _case(af, *case)
 
 
+# Seeded random configurations (drawn once, the same on every run): any head
+# dim, L a multiple of 16 up to 800, each mask with its block sizes, both
+# dtypes, scales up to 1/sqrt(D) (score spreads within the workloads').
+def _random_cases(seed=20261205, n=10):
+    import random
+    rnd = random.Random(seed)
+    cases = []
+    for _ in range(n):
+        mask = rnd.choice([DENSE, CAUSAL, BLOCK_DIAG])
+        D = 8 * rnd.randint(1, 32)
+        if mask == BLOCK_DIAG:
+            bs = rnd.choice([16, 32, 64, 128, 256])
+            L = bs * rnd.randint(1, max(1, 800 // bs))
+        else:
+            bs, L = 0, 16 * rnd.randint(1, 50)
+        dt = rnd.choice([torch.float16, torch.bfloat16])
+        scale = round(rnd.uniform(0.3, 1.0) / math.sqrt(D), 5)
+        cases.append((1, rnd.randint(1, 2), L, D, mask, bs, dt, scale, rnd.randint(0, 10 ** 6)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "B{}H{}L{}D{}m{}bs{}{}s{}".format(
+    *c[:6], "f16" if c[6] == torch.float16 else "bf16", c[7]))
+def test_fp8v_random_configurations(af, case):
+    B, H, L, D, mask, bs, dt, scale, seed = case
+    _case(af, B, H, L, D, mask, bs, dt, scale=scale, seed=seed)
+
+
 def test_fp8v_wide_scores(af):
     """N(0, 2^2) inputs: the running max moves often, so P is rounded against
     many different references and O is rescaled on most rows."""
