@@ -205,11 +205,18 @@ def fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, mask_kind: int 
         raise ValueError("q, k must be [B,H,L,D] and vt [B,H,D,L]")
     if vt.element_size() != 1:
         raise ValueError("vt must be float8 e5m2 (or its uint8 bytes)")
+    if k.dtype != q.dtype or k.device != q.device or vt.device != q.device:
+        raise ValueError("q, k (one dtype) and vt must be on one device")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     o = out if out is not None else torch.empty_like(q)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("out must be a contiguous tensor like q")
     lse = (lse_out if lse_out is not None else
            torch.empty((B, H, L), dtype=torch.float32, device=q.device)) if return_lse else None
+    if lse is not None and (tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32
+                            or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse_out must be a contiguous float32 [B, H, L] tensor on q's device")
     with torch.cuda.device(q.device):
         s = torch.cuda.current_stream(q.device)
         rc = lib.attn_fwd_fp8v(q.data_ptr(), k.data_ptr(), vt.data_ptr(), o.data_ptr(),
@@ -227,26 +234,37 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int =
     """Forward of HOST tensors through ``attn_fwd_host``: the library copies q,
     k, v to the GPU, runs the forward on the current stream of ``device``,
     copies o and lse back and synchronises, pipelined over chunks of heads
-    (``host_chunks``) so that both copy directions and the kernels overlap.  ``staging`` keeps the device
-    buffers (``q_d, k_d, v_d, o_d, lse_d``) and the page-locked host outputs
-    (``o_h, lse_h``) for reuse across calls.  Returns ``(o_host, lse_host)``."""
+    (``host_chunks``) so that both copy directions and the kernels overlap.
+    ``staging`` keeps the device buffers (``q_d, k_d, v_d, o_d, lse_d``) and the
+    page-locked host outputs (``o_h, lse_h``) for reuse by later calls of the
+    same shape, dtype and device (a call with others replaces them).  The
+    returned host tensors are those buffers: a later call with the same
+    ``staging`` overwrites them.  Returns ``(o_host, lse_host)``."""
     lib = load_library()
-    st = staging if staging is not None else {}
-    dev = torch.device("cuda", device)
-    for t in (q, k, v):
-        if t.device.type != "cpu" or not t.is_contiguous():
-            raise ValueError("fwd_host takes contiguous host tensors")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.device.type != "cpu" or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"fwd_host takes contiguous [B, H, L, D] host tensors ({name})")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
     B, H, L, D = (int(x) for x in q.shape)
+    dt = _dtype_code(q.dtype)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    for name in ("q_d", "k_d", "v_d", "o_d"):
-        if name not in st:
+    # staging buffers are reused only for the shape, dtype and device they were
+    # made for; any other call replaces them
+    st = staging if staging is not None else {}
+    key = (B, H, L, D, q.dtype, int(device))
+    if st.get("_key") != key:
+        dev = torch.device("cuda", device)
+        for name in ("q_d", "k_d", "v_d", "o_d"):
             st[name] = torch.empty(q.shape, dtype=q.dtype, device=dev)
-    if "lse_d" not in st:
         st["lse_d"] = torch.empty((B, H, L), dtype=torch.float32, device=dev)
-    if "o_h" not in st:
         st["o_h"] = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
         st["lse_h"] = torch.empty((B, H, L), dtype=torch.float32, pin_memory=True)
+        st["_key"] = key
+    dev = st["q_d"].device
     with torch.cuda.device(dev):
         s = torch.cuda.current_stream(dev)
         rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), st["o_h"].data_ptr(),
@@ -254,7 +272,7 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_kind: int =
                                st["q_d"].data_ptr(), st["k_d"].data_ptr(), st["v_d"].data_ptr(),
                                st["o_d"].data_ptr(), st["lse_d"].data_ptr(), B, H, L, D,
                                int(mask_kind), int(block_size), float(sm_scale),
-                               _dtype_code(q.dtype), ctypes.c_void_p(s.cuda_stream))
+                               dt, ctypes.c_void_p(s.cuda_stream))
     if rc:
         raise AttnError(rc, "attn_fwd_host")
     return st["o_h"], (st["lse_h"] if return_lse else None)
@@ -270,11 +288,22 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tens
     uint32/int32 tensor of one element that receives this call's device status
     once the current stream is synchronised.  The first call on a device does
     a one-time set-up and should come before any stream capture."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA [B, H, L, D] tensor")
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError(f"{name} must match q in shape, dtype and device")
+    B, H, L, D = (int(x) for x in q.shape)
+    if lse is not None and (tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32
+                            or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [B, H, L] tensor on q's device")
+    if status_out is not None and (status_out.device.type != "cpu" or status_out.numel() < 1
+                                   or status_out.element_size() != 4):
+        raise ValueError("status_out must be a host tensor of 4-byte elements")
     lib = load_library()
     fn = lib.attn_fwd_noalloc
     fn.restype = ctypes.c_int
     fn.argtypes = _SIGNATURES["attn_fwd"][1] + [ctypes.c_void_p]
-    B, H, L, D = (int(x) for x in q.shape)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
@@ -306,8 +335,8 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
             raise ValueError(f"{name} must match q in shape, dtype and device")
     B, H, L, D = (int(x) for x in q.shape)
     if (not lse.is_cuda or tuple(lse.shape) != (B, H, L) or lse.dtype != torch.float32
-            or not lse.is_contiguous()):
-        raise ValueError("lse must be a contiguous float32 CUDA [B, H, L] tensor")
+            or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [B, H, L] tensor on q's device")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     lib = load_library()
@@ -320,6 +349,8 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     need = int(lib.attn_bwd_workspace_size(B, H, L))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    elif workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on q's device")
     with torch.cuda.device(q.device):
         s = stream if stream is not None else torch.cuda.current_stream(q.device)
         rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),

@@ -218,3 +218,21 @@ def test_host_entry_point_rejections(lib):
     assert host(lse_h=P(32), lse_d=None) == 1
     assert host(lse_h=P(32), lse_d=P(20)) == 5
     assert host(B=0, h=(0, 0, 0, 0), d=(0, 0, 0, 0)) == 0
+
+
+def test_fwd_host_refuses_mismatched_inputs():
+    """fwd_host checks k and v against q (shape, dtype, layout) before any
+    CUDA call: the library copies q's byte count from each of them."""
+    import torch
+    import attention_forward_15_gb300 as af
+    q = torch.zeros((1, 2, 256, 64), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        af.fwd_host(q, q[:, :, :128].contiguous(), q)
+    with pytest.raises(ValueError):
+        af.fwd_host(q, q, q[:, :1].contiguous())
+    with pytest.raises(TypeError):
+        af.fwd_host(q, q.to(torch.bfloat16), q)
+    with pytest.raises(ValueError):
+        af.fwd_host(q, q.transpose(2, 3), q)
+    with pytest.raises(ValueError):
+        af.fwd_host(q[0], q[0], q[0])

@@ -297,6 +297,48 @@ def test_host_entry_point_large(af, B, H, L, D, mask, dt):
         assert torch.equal(o_h, o_ref.cpu()) and torch.equal(lse_h, lse_ref.cpu())
 
 
+def test_host_staging_follows_the_shape(af):
+    """One staging dict through calls of growing shapes and a dtype change:
+    each call gets buffers of its own shape (never the earlier, smaller ones)
+    and the bytes of attn_fwd on device buffers."""
+    dev = torch.device("cuda", 0)
+    staging = {}
+    for (B, H, L, D), dt in (((1, 2, 256, 64), torch.float16), ((2, 4, 640, 128), torch.float16),
+                             ((2, 4, 640, 128), torch.bfloat16), ((1, 2, 256, 64), torch.float16)):
+        q, k, v = (t.pin_memory() for t in make_qkv(B, H, L, D, dt, seed=B * L + D))
+        o_ref, lse_ref = af.fwd(q.to(dev), k.to(dev), v.to(dev), CAUSAL, 0, 0.1)
+        torch.cuda.synchronize()
+        o_h, lse_h = af.fwd_host(q, k, v, CAUSAL, 0, 0.1, staging=staging)
+        assert tuple(staging["q_d"].shape) == (B, H, L, D) and staging["q_d"].dtype == dt
+        assert torch.equal(o_h, o_ref.cpu()) and torch.equal(lse_h, lse_ref.cpu())
+
+
+def test_binding_refuses_mismatched_buffers(af):
+    """The binding checks every buffer against q before calling the library,
+    so a wrong shape, dtype or device never reaches a launch."""
+    dev = torch.device("cuda", 0)
+    q = torch.zeros((1, 2, 256, 64), dtype=torch.float16, device=dev)
+    short = torch.zeros((1, 2, 128, 64), dtype=torch.float16, device=dev)
+    lse = torch.zeros((1, 2, 256), dtype=torch.float32, device=dev)
+    with pytest.raises(ValueError):
+        af.fwd_noalloc(q, q, q, short, lse)
+    with pytest.raises(ValueError):
+        af.fwd_noalloc(q, short, q, q, lse)
+    with pytest.raises(ValueError):
+        af.fwd_noalloc(q, q, q, q, lse[:, :, :128])
+    with pytest.raises(ValueError):
+        af.fwd_noalloc(q, q, q, q.to(torch.bfloat16), lse)
+    vt = torch.zeros((1, 2, 64, 256), dtype=torch.uint8, device=dev)
+    with pytest.raises(ValueError):
+        af.fwd_fp8v(q, q, vt, out=short)
+    with pytest.raises(ValueError):
+        af.fwd_fp8v(q, q, vt, lse_out=lse[:, :, :128])
+    with pytest.raises(ValueError):
+        af.bwd(q, q, q, q, lse.cpu(), q)
+    with pytest.raises(ValueError):
+        af.bwd(q, q, q, q, lse, q, workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+
+
 def test_host_entry_point_stream_order(af):
     """attn_fwd_host on a non-default stream with work already queued on it:
     the library's copy streams start after that work (here a long fill of the
