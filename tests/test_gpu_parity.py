@@ -56,6 +56,16 @@ def _run(af, q, k, v, mask, bs, scale, guard=False):
     return o.cpu(), lse.cpu()
 
 
+def _row_ulps(err, ref, dtype):
+    """err in units of the last place of the 16-bit output at its row's largest
+    |O| (the output type's spacing there; subnormal spacing below the normal
+    range): an element near zero is measured against its row's scale."""
+    mant, emin = (10, -14) if dtype == torch.float16 else (7, -126)
+    row_max = np.abs(ref).reshape(-1, ref.shape[-1]).max(axis=1, keepdims=True)
+    e = np.floor(np.log2(np.maximum(row_max, 2.0 ** emin)))
+    return err.reshape(-1, ref.shape[-1]) / np.exp2(e - mant)
+
+
 def _check(o, lse, O_ref, lse_ref, dtype, what, o_scale=1.0):
     og = o.double().numpy().reshape(O_ref.shape)
     lg = lse.double().numpy().reshape(lse_ref.shape)
@@ -63,6 +73,11 @@ def _check(o, lse, O_ref, lse_ref, dtype, what, o_scale=1.0):
     assert np.isfinite(lg).all(), f"{what}: non-finite lse"
     eo = np.abs(og - O_ref).max() if og.size else 0.0
     el = np.abs(lg - lse_ref).max() if lg.size else 0.0
+    if og.size:
+        # the GPU rounds P to the 16-bit type before P.V (the oracle does not):
+        # reported, in output ulps, beside the bound
+        print(f"{what}: max|dO| {eo:.3e} ({_row_ulps(np.abs(og - O_ref), O_ref, dtype).max():.2f} ulps of the "
+              f"row's largest output), max|dlse| {el:.3e}")
     tol = TOL_O[dtype] * o_scale
     assert eo <= tol, f"{what}: max|dO| = {eo:.3e} > {tol}"
     assert el <= TOL_LSE, f"{what}: max|dlse| = {el:.3e} > {TOL_LSE}"
