@@ -24,7 +24,7 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     unsigned int *status = nullptr;   // device status word written by timed-out waits
-    bool smem_attr[6][2] = {};        // per (kernel, dtype): dynamic smem attribute set
+    bool smem_attr[9][2] = {};        // per (kernel, dtype): dynamic smem attribute set
     bool bwd_attr[3][2][2] = {};      // backward: per (head dim, dtype, dK/dV | dQ)
     // backward: a second stream for the dQ kernel, forked from and joined back
     // into the caller's stream by two events (created on the first backward)
@@ -45,6 +45,11 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool head_dim_ok(int D) { return D >= 8 && D <= 256 && D % 8 == 0; }
 int kernel_dim(int D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
 int head_dim_index(int D) { return kernel_dim(D) == 64 ? 0 : (kernel_dim(D) == 128 ? 1 : 2); }
+// Block-diagonal with blocks of at most 64 keys: every key tile is masked and
+// a row attends one 64-key half of it (the one-half instantiations).
+bool small_blocks(int mask_kind, int block_size) {
+    return mask_kind == ATTN_MASK_BLOCK_DIAG && block_size <= 64;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -191,14 +196,17 @@ int encode_map_vt8(CUtensorMap *m, const void *ptr, int BH, int L, int D, int ro
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <int D, bool BF16, bool PAIR, bool FP8V = false>
+// BDH: the block-diagonal instantiation for blocks of at most 64 keys (D <= 128,
+// 16-bit P), chosen by the callers below.
+template <int D, bool BF16, bool PAIR, bool FP8V = false, bool BDH = false>
 int launch(DeviceState &st, const void *q, const void *k, const void *v, FwdParams prm, int dtype,
            cudaStream_t stream) {
+    static_assert(!BDH || (D <= 128 && !FP8V), "one-half block-diagonal kernels: D <= 128, 16-bit P");
     using C = Cfg<D, PAIR, FP8V>;
-    auto kern = attn::attn_fwd_kernel<D, BF16, PAIR, FP8V>;
+    auto kern = attn::attn_fwd_kernel<D, BF16, PAIR, FP8V, BDH>;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
-        bool &set = st.smem_attr[head_dim_index(D) + (FP8V ? 3 : 0)][BF16 ? 1 : 0];
+        bool &set = st.smem_attr[head_dim_index(D) + (FP8V ? 3 : 0) + (BDH ? 6 : 0)][BF16 ? 1 : 0];
         if (!set) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM_BYTES) != cudaSuccess)
@@ -365,6 +373,13 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == ATTN_BF16;
+    if constexpr (!FP8V) {
+        if (small_blocks(mask_kind, block_size) && kernel_dim(D) <= 128)
+            return kernel_dim(D) == 64 ? (bf16 ? launch<64, true, true, false, true>(*st, q, k, v, prm, dtype, s)
+                                               : launch<64, false, true, false, true>(*st, q, k, v, prm, dtype, s))
+                                       : (bf16 ? launch<128, true, true, false, true>(*st, q, k, v, prm, dtype, s)
+                                               : launch<128, false, true, false, true>(*st, q, k, v, prm, dtype, s));
+    }
     switch (kernel_dim(D)) {
         case 64:
             return bf16 ? launch<64, true, true, FP8V>(*st, q, k, v, prm, dtype, s)
@@ -517,14 +532,19 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *v, voi
     prm.d_out = D;
 
     const bool bf16 = dtype == ATTN_BF16;
+    const bool bdh = small_blocks(mask_kind, block_size);
     switch (kernel_dim(D)) {
         case 64:
-            rc = bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
-                      : launch<64, false, true>(*st, q, k, v, prm, dtype, s);
+            rc = bdh ? (bf16 ? launch<64, true, true, false, true>(*st, q, k, v, prm, dtype, s)
+                             : launch<64, false, true, false, true>(*st, q, k, v, prm, dtype, s))
+                     : (bf16 ? launch<64, true, true>(*st, q, k, v, prm, dtype, s)
+                             : launch<64, false, true>(*st, q, k, v, prm, dtype, s));
             break;
         case 128:
-            rc = bf16 ? launch<128, true, true>(*st, q, k, v, prm, dtype, s)
-                      : launch<128, false, true>(*st, q, k, v, prm, dtype, s);
+            rc = bdh ? (bf16 ? launch<128, true, true, false, true>(*st, q, k, v, prm, dtype, s)
+                             : launch<128, false, true, false, true>(*st, q, k, v, prm, dtype, s))
+                     : (bf16 ? launch<128, true, true>(*st, q, k, v, prm, dtype, s)
+                             : launch<128, false, true>(*st, q, k, v, prm, dtype, s));
             break;
         default:
             rc = bf16 ? launch<256, true, false>(*st, q, k, v, prm, dtype, s)

@@ -501,7 +501,9 @@ __device__ __forceinline__ void exp_pack8(const uint32_t *v, float sc, float neg
 // ([B*H, D, L], keys innermost), P is rounded to e5m2 and P.V runs as a
 // kind::f8f6f4 MMA; the reference max is the exact running max (threshold 0),
 // so P is rounded against the same max as the page's recurrence.
-template <int D, bool BF16, bool PAIR, bool FP8V = false>
+// BDH: the block-diagonal instantiation for blocks of at most 64 keys, whose
+// masked tiles read and exponentiate only the half of the tile a row attends.
+template <int D, bool BF16, bool PAIR, bool FP8V = false, bool BDH = false>
 __global__ void __launch_bounds__(Cfg<D, PAIR, FP8V>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
@@ -1219,8 +1221,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     if (!done) {
                         // Pass 1: row extreme (max for sm_scale >= 0, else min) over the
                         // two 64-key halves; the upper half stays in registers.
+                        // one_half: block-diagonal with blocks of at most 64 keys, where
+                        // a row's keys lie in one 64-key half of the tile, the same half
+                        // for every row of the warp (blocks never straddle key 64 and a
+                        // warp's 32 rows share one 64-row block): only that half (hv) is
+                        // read and exponentiated, and the other half's P is zero.
+                        const bool one_half = BDH && masked && p.mask == kMaskBlock && p.bs <= 64;
+                        const int hv = one_half && rel_lo < 64 ? 0 : 1;   // the half held in hi
                         uint32_t hi[64];
                         float ext;
+                        if (one_half) {
+                            tmem_ld32(s_addr + 64 * hv, *reinterpret_cast<uint32_t(*)[32]>(hi));
+                            tmem_ld32(s_addr + 64 * hv + 32, *reinterpret_cast<uint32_t(*)[32]>(hi + 32));
+                            tmem_wait_ld();
+                            if constexpr (C::SEP) {
+                                // last read of this S: the MMA warp may overwrite it now
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(bar(C::B_SFREE + wg));
+                            }
+                            mask_half(hi, 64 * hv, rel_lo, rel_hi, fill);
+                            ext = row_extreme64(hi, sc >= 0.f);
+                        } else {
                         {
                             uint32_t lo[64];
                             tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
@@ -1237,6 +1259,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         {
                             const float e2 = row_extreme64(hi, sc >= 0.f);
                             ext = sc >= 0.f ? fmaxf(ext, e2) : fminf(ext, e2);
+                        }
                         }
                         const float m_tile = isinf(ext) ? -INFINITY : ext * sc;
                         if (t == 0) {
@@ -1264,10 +1287,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         // (the element-wise mask exists only in the masked instantiation,
                         // chosen once per tile)
                         if (masked)
-                            exp_half_any<BF16, true, FP8V>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
+                            exp_half_any<BF16, true, FP8V>(hi, 64 * hv, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
                         else
                             exp_half_any<BF16, false, FP8V>(hi, 64, rel_lo, rel_hi, sc, neg_m, acc, p_addr, p8_addr);
-                        {
+                        if (one_half) {
+                            // zeros for the other half's P (16-bit pairs: 32 columns;
+                            // e5m2 quads: 16 columns)
+                            if constexpr (FP8V) {
+                                tmem_st16_zero(p8_addr + 16 * (1 - hv));
+                            } else {
+                                tmem_st16_zero(p_addr + 32 * (1 - hv));
+                                tmem_st16_zero(p_addr + 32 * (1 - hv) + 16);
+                            }
+                        } else {
                             uint32_t lo[64];
                             tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(lo));
                             tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(lo + 32));

@@ -399,6 +399,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+// 16 columns of zeros (one zero register for every operand of the store).
+__device__ __forceinline__ void tmem_st16_zero(uint32_t taddr) {
+    asm volatile(
+        "{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {z, z, z, z, z, z, z, z, z, z, z, z, z, z, z, z};\n\t}"
+        ::"r"(taddr)
+        : "memory");
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor of a tcgen05 operand stored with the
