@@ -36,10 +36,11 @@ def lib():
 CASES = [(2, 4, 640, 128, CAUSAL, 0, torch.bfloat16),
          (1, 4, 512, 64, DENSE, 0, torch.float16),
          (1, 2, 512, 256, DENSE, 0, torch.bfloat16),
-         (1, 2, 384, 128, BLOCK_DIAG, 64, torch.float16)]
+         (1, 2, 384, 128, BLOCK_DIAG, 64, torch.float16),
+         (1, 2, 256, 64, BLOCK_DIAG, 16, torch.bfloat16)]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "L{}D{}m{}".format(c[2], c[3], c[4]))
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "L{}D{}m{}bs{}".format(c[2], c[3], c[4], c[5]))
 def test_noalloc_matches_regular_entry_point(lib, case):
     import attention_forward_15_gb300 as af
     B, H, L, D, mask, bs, dt = case
