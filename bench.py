@@ -493,10 +493,14 @@ def main():
             steps2 = max(5, min(args.steps, int(2e12 / f2) + 5, 200))
             ms2, _ = time_workload(af, ow, dev, steps2, 3)
             rl = roofline_for(ow, f2, b2, ms2, peaks, peaks_kind, ncu_traffic(name))
+            # end to end through the host-buffer call, as for the main line
+            e2e2, _, _ = time_e2e(af, ow, dev, 10, 2)
             per_mask[name] = {"mask": MASK_NAMES[ow.mask], "ms": round(ms2, 4),
                               "tflops": round(f2 / (ms2 * 1e-3) / 1e12, 2),
                               "roofline_bound": rl["bound"], "roofline_frac": rl["frac"],
-                              "achieved": rl["achieved"], "unit": rl["unit"]}
+                              "achieved": rl["achieved"], "unit": rl["unit"],
+                              "e2e_ms": round(e2e2 * 1e3, 4),
+                              "e2e_tflops": round(f2 / e2e2 / 1e12, 2)}
     # The FP8 P.V variant (V as e5m2, P rounded to e5m2) on three workloads.
     fp8_pv = {}
     if not args.no_all:
